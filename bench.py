@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Benchmark of context-parallel MLA prefill attention on GB300.
+
+One step = the whole path over one batch: DualChunkSwap partition maps (built
+once per batch, outside the device-timed region), partial attention of all P
+virtual shards in one launch, then the global LSE merge with the sink and the
+restore to global order.  Default workload: one 8192-token request, 16 heads,
+P = 2, dense causal (the configuration the headline metric is quoted on).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl cuda|reference] [--no-cpu-baseline]
+
+Prints one JSON line.  value = TFLOP/s of the step (2*576 + 2*512 flops per
+attended (token, head, key)), inputs resident in HBM, L2 flushed between steps.
+e2e = the same metric through the public API with pinned host buffers: host
+partition, host->device copy of the step's inputs, attention, merge, and the
+device->host copy of the output inside the timed region.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 roofline"
+FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(prob, target_s=12.0, max_tokens=4096, seed=0):
+    """Time the fp64 oracle on a bounded seeded sample of the workload's tokens
+    (all heads each); returns (TFLOP/s, tokens/s, n_tokens, seconds, cores)."""
+    from oracle import oracle as orc
+    from tests import parity_util as pu
+    orc.build()
+    kvh = pu.kv_host(prob)
+    pos_all = prob.token_pos().numpy()
+    rng = np.random.default_rng(seed)
+
+    def run(n):
+        toks = np.sort(rng.choice(prob.T, size=min(n, prob.T), replace=False))
+        keys = np.minimum(pos_all[toks].astype(np.int64) + 1, prob.topk) if prob.topk else \
+            pos_all[toks].astype(np.int64) + 1
+        t0 = time.perf_counter()
+        pu.oracle_tokens(prob, toks, kvh=kvh)
+        dt = time.perf_counter() - t0
+        return len(toks), float(keys.sum()) * prob.H * FLOPS_PER_KEY_HEAD, dt
+
+    n0, f0, d0 = run(16)
+    n = int(min(max_tokens, max(16, 16 * target_s / max(d0, 1e-3))))
+    n1, f1, d1 = run(n)
+    cores = os.cpu_count()
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        pass
+    omp = os.environ.get("OMP_NUM_THREADS")
+    if omp:
+        cores = min(cores, int(omp))
+    return f1 / d1 / 1e12, n1 / d1, n1, d1, cores
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="dense_s8192_h16_p2")
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    world, rank, local = dist_setup(args.gpus)
+    from context_sparse_mla_gb300 import synth
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    from context_sparse_mla_gb300 import build as cbuild
+    from context_sparse_mla_gb300 import cpmla
+    cbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    prob = synth.make_problem(args.workload, device=dev, seed=args.seed)
+    flops = synth.attended_keys(prob) * prob.H * FLOPS_PER_KEY_HEAD
+    tokens = prob.T
+    plan = cpmla.plan_for(prob, device=dev)
+    kvk = cpmla.kv_kwargs(prob)
+    o_out = torch.empty((prob.T, prob.H, 512), dtype=torch.bfloat16, device=dev)
+    lse_out = torch.empty((prob.T, prob.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        plan.attention(prob.q, softmax_scale=prob.scale, idx=prob.idx, stream=stream, **kvk)
+        if ev:
+            ev[1].record(stream)
+        plan.merge(o_out, lse_out, sink=prob.sink, stream=stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))  # evict L2 between steps (outside the events)
+            step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    status = cpmla.device_status()
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    merge_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = sum(a + m for a, m in zip(attn_ms, merge_ms)) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    merge_avg = sum(merge_ms) / len(merge_ms)
+
+    # ---------------- end to end through the public API with host buffers
+    q_h = prob.q.cpu().pin_memory()
+    kv_h = {k: v.cpu().pin_memory() for k, v in kvk.items()}
+    sink_h = prob.sink.cpu().pin_memory()
+    idx_h = prob.idx.cpu().pin_memory() if prob.idx is not None else None
+    o_h = torch.empty((prob.T, prob.H, 512), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((prob.T, prob.H), dtype=torch.float32).pin_memory()
+    cu, qs, dec, kvs = (prob.cu_seqlens.numpy(), prob.q_start_pos.numpy(), prob.is_decode.numpy(),
+                        prob.kv_start.numpy())
+    q_d = torch.empty_like(prob.q)
+    kv_d = {k: torch.empty_like(v) for k, v in kvk.items()}
+    sink_d = torch.empty_like(prob.sink)
+    idx_d = torch.empty_like(prob.idx) if prob.idx is not None else None
+    h2d = q_h.numel() * 2 + sum(v.numel() * v.element_size() for v in kv_h.values()) + sink_h.numel() * 4
+    if idx_h is not None:
+        h2d += idx_h.numel() * 4
+    d2h = o_h.numel() * 2 + lse_h.numel() * 4
+
+    def e2e_step():
+        p = cpmla.PcpPrefill(prob.P, cu, qs, dec, kvs, prob.H, device=dev, topk=prob.topk)
+        q_d.copy_(q_h, non_blocking=True)
+        for k in kv_d:
+            kv_d[k].copy_(kv_h[k], non_blocking=True)
+        sink_d.copy_(sink_h, non_blocking=True)
+        if idx_d is not None:
+            idx_d.copy_(idx_h, non_blocking=True)
+        p(q_d, softmax_scale=prob.scale, sink=sink_d, idx=idx_d, o_out=o_out, lse_out=lse_out,
+          stream=stream, **kv_d)
+        o_h.copy_(o_out, non_blocking=True)
+        lse_h.copy_(lse_out, non_blocking=True)
+        torch.cuda.synchronize()
+        return p
+
+    for _ in range(2):
+        e2e_step()
+    # the partition maps' uploads are part of the step too
+    maps_bytes = sum(getattr(e2e_step(), k).numel() * 4 for k in ("rows", "pos", "req", "owner_row"))
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        flush.fill_(2.0)
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world)
+
+    # ---------------- roofline (attention kernel) and merge bandwidth
+    pk = peaks()
+    attn_tflops = flops / (attn_avg * 1e-3) / 1e12
+    n_part = plan.n_rows
+    merge_bytes = n_part * prob.H * (512 * 4 + 4) + prob.T * prob.H * (512 * 2 + 4) + \
+        prob.T * 4 + prob.H * 4
+    merge_gbs = merge_bytes / (merge_avg * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, tps, n_tok, secs, cores = cpu_oracle_sample(prob)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": "%d of %d tokens of the workload (all %d heads each), seeded, %.1f s; "
+                         "%.1f tokens/s" % (n_tok, prob.T, prob.H, secs, tps)}
+
+    value = world * flops / (step_ms * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/KV, N(0,1) sink; no dataset or weights)",
+        "config": {"workload": args.workload, "tokens": tokens, "heads": prob.H, "pcp": prob.P,
+                   "topk": prob.topk, "kv_format": prob.kv_format,
+                   "l2": "flushed between steps (512 MiB write)", "parallelism": "replicas"
+                   if world > 1 else "single GPU, %d virtual PCP shards" % prob.P},
+        "tokens_per_s": round(world * tokens / (step_ms * 1e-3), 1),
+        "attn_ms": round(attn_avg, 4), "merge_ms": round(merge_avg, 4),
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
+                     "peak": pk["bf16"], "unit": "TFLOP/s",
+                     "frac": round(attn_tflops / pk["bf16"], 4), "traffic": None,
+                     "kernel": "mla_attn_kernel", "peak_source": pk["source"] + " burst bf16"},
+        "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm"],
+                           "unit": "GB/s", "frac": round(merge_gbs / pk["hbm"], 4),
+                           "bytes": merge_bytes},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d + maps_bytes,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+        "wall_s_timed": round(t_wall, 3),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands on the host cores, on a bounded sample per step."""
+    from context_sparse_mla_gb300 import synth
+    if rank != 0:
+        return
+    prob = synth.make_problem(args.workload, device="cpu", seed=args.seed) \
+        if args.workload in ("dense_s256_h4_p2", "dense_s8192_h16_p2") else \
+        synth.make_problem(args.workload, device="cuda", seed=args.seed)
+    per_step = []
+    total_tf = []
+    n_tok = 0
+    for i in range(args.warmup + args.steps):
+        tf, tps, n_tok, secs, cores = cpu_oracle_sample(prob, target_s=1.0, max_tokens=512,
+                                                        seed=i)
+        if i >= args.warmup:
+            per_step.append(secs)
+            total_tf.append(tf)
+    value = statistics.median(total_tf)
+    out = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(1e3 * statistics.median(per_step), 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": args.workload}, "impl": "reference",
+           "cpu_baseline": {"kind": "oracle", "cores": cores, "value": round(value, 6),
+                            "unit": "TFLOP/s",
+                            "sample": "%d tokens per step (all heads), seeded" % n_tok},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * cpmla.h -- C ABI of libcpmla.so: context-parallel (PCP) prefill attention
+ * over MLA latent KV on one GB300 (sm_103a).
+ *
+ * The path (one call each, in this order):
+ *   1. pcp_dualchunk_partition   host: DualChunkSwap split into P virtual shards
+ *   2. mla_partial_attn_dense /  device: per-shard partial attention (O, LSE)
+ *      mla_partial_attn_sparse           over the full latent KV, no sink
+ *   3. lse_merge_with_sink       device: global LSE merge, sink applied once,
+ *                                         output written in global token order
+ *
+ * Conventions shared by every entry point
+ *   - Return value: CPMLA_OK (0) or a negative CPMLA_ERR_* code.  On error the
+ *     calling thread's message is available from cpmla_last_error().  Nothing
+ *     is launched when argument checks fail.
+ *   - Ownership: every pointer is owned by the caller; the library never
+ *     allocates, frees or retains memory.  "host" pointers are read/written
+ *     during the call only; "device" pointers must be valid on the current
+ *     CUDA device until the work queued on `stream` has finished.
+ *   - Device entry points are asynchronous on `stream` (a cudaStream_t passed
+ *     as void*, NULL = legacy default stream).  Launch errors are reported
+ *     immediately as CPMLA_ERR_CUDA.  Faults detected inside a kernel (an index
+ *     outside its row's causal prefix, a bounded wait that ran out) are
+ *     recorded in a per-device status word read with cpmla_device_status().
+ *   - Element types: bf16 = IEEE bfloat16 stored as uint16; fp8 = OCP E4M3
+ *     stored as uint8; LSE values are natural-log fp32, -inf for a row with no
+ *     key.
+ *   - Head dims are fixed by the model family: D_qk = 576 (512 latent + 64
+ *     rope, absorbed), D_v = 512 (the latent, which is also the value).
+ */
+#ifndef CPMLA_H
+#define CPMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  CPMLA_OK = 0,
+  CPMLA_ERR_ARG = -1,         /* bad argument (null, size, alignment, range) */
+  CPMLA_ERR_CUDA = -2,        /* a CUDA runtime call or launch failed */
+  CPMLA_ERR_UNSUPPORTED = -3, /* valid request this build does not implement */
+  CPMLA_ERR_TIMEOUT = -4,     /* status word: a bounded device wait ran out */
+  CPMLA_ERR_INDEX = -5        /* status word: an index outside its row's range */
+};
+
+/* KV cache layouts. */
+enum {
+  /* kv: bf16 [S_kv, 576], row stride 576 elements, 16-byte aligned. */
+  CPMLA_KV_BF16 = 0,
+  /* kv_fp8: E4M3 latent [S_kv, 512]; kv_scale: fp32 [S_kv, 4], one scale per
+   * 128 latent channels (value = e4m3 * scale); kv_rope: bf16 [S_kv, 64].
+   * The pages name an fp8 MLA cache ("fp8_ds_mla") without a layout; this
+   * one is the library's own. */
+  CPMLA_KV_FP8_E4M3_G128 = 1
+};
+
+#define CPMLA_DQK 576
+#define CPMLA_DV 512
+#define CPMLA_DROPE 64
+
+/* Thread-local message for the last error returned on this thread ("" if none). */
+const char *cpmla_last_error(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int cpmla_version(void);
+
+/*
+ * Reads (and, if clear != 0, resets) the device-side status word of the
+ * current device: CPMLA_OK, CPMLA_ERR_INDEX or CPMLA_ERR_TIMEOUT (the first
+ * fault recorded since the last reset).  Synchronises the current device.
+ */
+int cpmla_device_status(int *status, int clear);
+
+/* --------------------------------------------------------------------------
+ * 1. DualChunkSwap partition (host)
+ *
+ * "[Core] Add MRV2 virtual-batch PCP for MLA", sections "PCP algorithm" and
+ * "DualChunkSwap partitioning" (PCP=4 diagram): each prefill request is cut
+ * into 2P contiguous chunks and virtual shard r takes chunks r and 2P-1-r;
+ * each prefill is partitioned on its own; decode rows are replicated on every
+ * shard.  Where the page is silent: chunk c of an S-token request has
+ * floor(S/2P) tokens plus one when c < S mod 2P; inside a shard the rows go by
+ * request in input order, then chunk r before chunk 2P-1-r, ascending; a
+ * replicated decode row is owned by shard 0.
+ *
+ * Inputs (host):
+ *   P             number of virtual shards, 1..1024
+ *   B             number of requests, >= 0
+ *   cu_seqlens    [B+1] non-decreasing global token offsets, cu_seqlens[0]=0
+ *   q_start_pos   [B] position of each request's first scheduled token
+ *                 (0 for a fresh prefill; context length - 1 for a decode)
+ *   is_decode     [B] 1 = decode request (replicated on all shards), else 0
+ * Outputs (host, caller-allocated; sizes from pcp_partition_size):
+ *   shard_offsets [P+1] shard r owns rows [shard_offsets[r], shard_offsets[r+1])
+ *   rows, pos, req [n_rows_total] global token id, request-local position and
+ *                 request index of each shard row (all shards concatenated)
+ *   owner_shard, owner_row [T = cu_seqlens[B]] for every global token the
+ *                 shard and the concatenated row index whose result is kept
+ * Errors: CPMLA_ERR_ARG (null pointer, P out of range, decreasing offsets,
+ * negative position, sizes beyond int32).
+ * ------------------------------------------------------------------------ */
+int pcp_partition_size(int P, int B, const int32_t *cu_seqlens, const uint8_t *is_decode,
+                       int64_t *n_rows_total);
+
+int pcp_dualchunk_partition(int P, int B, const int32_t *cu_seqlens, const int32_t *q_start_pos,
+                            const uint8_t *is_decode, int32_t *shard_offsets, int32_t *rows,
+                            int32_t *pos, int32_t *req, int32_t *owner_shard,
+                            int32_t *owner_row);
+
+/* --------------------------------------------------------------------------
+ * 2. Per-shard partial MLA attention (device)
+ *
+ * "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
+ * MegaMoE", "Implementation summary": each PCP rank computes local partial
+ * attention and hands (output, LSE) to a global merge; "[Core] Add MRV2
+ * virtual-batch PCP for MLA", "DualChunkSwap partitioning": the latent KV is
+ * all-gathered so every shard sees the full KV.  No sink is applied here.
+ *
+ * For shard row i (global token g = rows[i], position t = pos[i], request
+ * b = req[i]) and head h, with key set J_i:
+ *   s_j    = softmax_scale * q[g,h,:] . kv[kv_start[b] + j, :]   (576 wide)
+ *   lse    = ln sum_{j in J_i} exp(s_j)
+ *   o_part = sum_{j in J_i} exp(s_j - lse) * kv[kv_start[b] + j, 0:512]
+ * J_i = {0..t} (dense) or the entries >= 0 of topk_idx[g, 0..k-1] (sparse),
+ * intersected with [kv_lo[i], kv_hi[i]] when those arrays are given.
+ *
+ * Arguments (device unless noted):
+ *   q            bf16 [T, H, 576]; token g's head h starts at
+ *                q + g*q_token_stride + h*576 (elements); 16-byte aligned
+ *   q_token_stride  elements between tokens, >= H*576, multiple of 8 (host)
+ *   H            heads, 1..128; if H > 64 it must be a multiple of 64 (host)
+ *   kv_format    CPMLA_KV_* (host).  Dense accepts CPMLA_KV_BF16 only.
+ *   kv / kv_fp8, kv_scale, kv_rope   per kv_format (unused ones may be NULL)
+ *   s_kv         KV rows (host); every key read lies in [0, s_kv)
+ *   kv_start     int64 [B] KV row of request b's position 0
+ *   rows, pos, req  int32 [n_rows] as produced by pcp_dualchunk_partition
+ *   n_rows       shard rows to compute (host); 0 is a no-op
+ *   kv_lo, kv_hi int32 [n_rows] or NULL: inclusive position range a row may use
+ *   topk_idx     int32 [T, k] (sparse) request-local key positions by global
+ *                token, -1 = empty slot; an entry outside 0..t is skipped and
+ *                recorded as CPMLA_ERR_INDEX in the status word
+ *   k            top-k width (host), 1..65536
+ *   softmax_scale  (host), finite and > 0
+ *   o_part       fp32 [n_rows, H, 512] output; lse_part fp32 [n_rows, H] output
+ * Errors: CPMLA_ERR_ARG, CPMLA_ERR_UNSUPPORTED, CPMLA_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int mla_partial_attn_dense(const void *q, int64_t q_token_stride, int H, int kv_format,
+                           const void *kv, const void *kv_fp8, const float *kv_scale,
+                           const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                           const int32_t *rows, const int32_t *pos, const int32_t *req,
+                           int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+                           float softmax_scale, float *o_part, float *lse_part, void *stream);
+
+int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, int H, int kv_format,
+                            const void *kv, const void *kv_fp8, const float *kv_scale,
+                            const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                            const int32_t *rows, const int32_t *pos, const int32_t *req,
+                            int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+                            const int32_t *topk_idx, int k, float softmax_scale, float *o_part,
+                            float *lse_part, void *stream);
+
+/* --------------------------------------------------------------------------
+ * 3. Global LSE merge + attention sink once + restore to global order (device)
+ *
+ * "[DeepSeekV4][PCP] ...", "Implementation summary" (merge LSE/output
+ * globally, apply attn_sink only once) and "Main challenges" (attn_sink must
+ * not be applied on each rank); "[Core] Add MRV2 virtual-batch PCP for MLA",
+ * "DualChunkSwap partitioning" (restore to global scheduled-token order).
+ * The sink is read as one extra logit per head with a zero value vector.
+ *
+ * For global token g and head h, with partial rows c in C_g:
+ *   L   = ln sum_c exp(lse_part[c,h])
+ *   O   = sum_c exp(lse_part[c,h] - L) * o_part[c,h,:]
+ *   O  *= 1 / (1 + exp(sink[h] - L))          (skipped when sink == NULL)
+ *   o_out[g,h,:] = bf16(O),  lse_out[g,h] = L (the sink is not folded in)
+ * A token whose partials are all empty (lse = -inf) gets O = 0, L = -inf.
+ *
+ * Arguments (device unless noted):
+ *   o_part fp32 [n_part, H, 512], 16-byte aligned; lse_part fp32 [n_part, H]
+ *   n_part, H, T  sizes (host); H 1..1024
+ *   contrib_off  int32 [T+1] CSR offsets into contrib_rows, or NULL meaning
+ *                exactly one partial per token: C_g = {contrib_rows[g]}
+ *   contrib_rows int32 partial-row indices in [0, n_part)
+ *   sink         fp32 [H] or NULL
+ *   o_out        bf16 [T, H, 512] output (16-byte aligned); lse_out fp32 [T, H]
+ * Errors: CPMLA_ERR_ARG, CPMLA_ERR_CUDA.  A contrib row outside [0, n_part)
+ * is skipped and recorded as CPMLA_ERR_INDEX in the status word.
+ * ------------------------------------------------------------------------ */
+int lse_merge_with_sink(const float *o_part, const float *lse_part, int64_t n_part, int H,
+                        const int32_t *contrib_off, const int32_t *contrib_rows, int T,
+                        const float *sink, void *o_out, float *lse_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPMLA_H */

@@ -1,0 +1,204 @@
+"""GPU parity: the CUDA path (partition -> partial attention -> merge with sink,
+all through the C ABI) against the fp64 oracle, element by element, on seeded
+inputs.  Small cases compare every token; the full-size workloads compare a
+seeded sample of >= 4096 tokens (all heads, all 512 channels each) in the same
+launch configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+from context_sparse_mla_gb300 import build as cbuild
+from context_sparse_mla_gb300 import cpmla, synth
+from oracle import oracle as orc
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    cbuild.build()
+    cpmla.lib()
+    cpmla.device_status(clear=True)
+    yield
+    torch.cuda.synchronize()
+
+
+def _check_all(prob):
+    o, lse, _ = pu.run_path(prob)
+    toks = np.arange(prob.T)
+    ro, rl = pu.oracle_tokens(prob, toks)
+    return pu.compare(o, lse, ro, rl)
+
+
+def _check_sample(prob, n, seed=0):
+    o, lse, _ = pu.run_path(prob)
+    toks = pu.sample_tokens(prob, n, seed)
+    ro, rl = pu.oracle_tokens(prob, toks)
+    ti = torch.as_tensor(toks, device=o.device)
+    return pu.compare(o[ti], lse[ti], ro, rl)
+
+
+# ----------------------------------------------------------------- dense
+def test_dense_tiny_workload_every_token():
+    prob = synth.make_problem("dense_s256_h4_p2", device="cuda")
+    _check_all(prob)
+
+
+def test_dense_ragged_multi_tile_every_token():
+    prob = synth.make_problem("dense_s8192_h16_p2", S=1000, device="cuda", seed=3)
+    _check_all(prob)
+
+
+@pytest.mark.parametrize("H", [1, 5, 32, 64, 128])
+def test_dense_head_groupings(H):
+    prob = synth.make_problem("dense_s8192_h16_p2", S=300, H=H, P=3, device="cuda", seed=H)
+    _check_all(prob)
+
+
+def test_dense_varlen_with_decode_rows():
+    prob = synth.make_problem("varlen_p8_h64", prefill_lens=[700, 5, 260], decode_ctx=[900, 33],
+                              H=8, P=3, topk=0, device="cuda", seed=5)
+    _check_all(prob)
+
+
+def test_dense_fewer_tokens_than_chunks():
+    prob = synth.make_problem("dense_s256_h4_p2", S=5, P=4, device="cuda", seed=8)
+    _check_all(prob)
+
+
+# ----------------------------------------------------------------- sparse
+def test_sparse_bf16_h32_p4():
+    prob = synth.make_problem("sparse_s32k_h32_p4", S=3000, device="cuda", seed=1)
+    _check_sample(prob, 300)
+
+
+def test_sparse_fp8_h16_p2():
+    prob = synth.make_problem("sparse_s128k_h16_p2_fp8", S=2600, device="cuda", seed=2)
+    _check_sample(prob, 300)
+
+
+def test_sparse_varlen_h64_p8_decode():
+    prob = synth.make_problem("varlen_p8_h64", prefill_lens=[2500, 1100], decode_ctx=[4100, 9000],
+                              device="cuda", seed=4)
+    _check_sample(prob, 200)
+
+
+@pytest.mark.parametrize("H", [1, 16, 24])
+def test_sparse_unsorted_lists_with_holes(H):
+    """Top-k lists need not be sorted and may hold -1 anywhere."""
+    prob = synth.make_problem("sparse_s32k_h32_p4", S=700, H=H, topk=200, device="cuda", seed=H)
+    g = torch.Generator(device="cuda").manual_seed(11)
+    idx = prob.idx.clone()
+    perm = torch.argsort(torch.rand(idx.shape, generator=g, device="cuda"), dim=1)
+    idx = torch.gather(idx, 1, perm)
+    holes = torch.rand(idx.shape, generator=g, device="cuda") < 0.2
+    holes[:, 0] = False
+    idx[holes & (torch.arange(idx.shape[0], device="cuda")[:, None] > 0)] = -1
+    prob.idx = idx.contiguous()
+    _check_all(prob)
+
+
+def test_sparse_out_of_prefix_index_is_skipped_and_flagged():
+    prob = synth.make_problem("sparse_s32k_h32_p4", S=400, H=16, topk=64, device="cuda", seed=6)
+    bad_tok = 300
+    idx = prob.idx.clone()
+    idx[bad_tok, 0] = 350  # outside [0, 300]
+    prob.idx = idx
+    plan = cpmla.plan_for(prob)
+    o, lse = plan(prob.q, softmax_scale=prob.scale, sink=prob.sink, idx=prob.idx,
+                  **cpmla.kv_kwargs(prob))
+    assert cpmla.device_status(clear=True) == cpmla.CPMLA_ERR_INDEX
+    fixed = idx.clone()
+    fixed[bad_tok, 0] = -1
+    prob.idx = fixed
+    ro, rl = pu.oracle_tokens(prob, [bad_tok])
+    pu.compare(o[bad_tok:bad_tok + 1], lse[bad_tok:bad_tok + 1], ro, rl)
+
+
+# ----------------------------------------------------------------- merge
+def test_kv_split_partials_merge_to_full_attention():
+    """General N-partial merge: every row's keys split into the 2P DualChunkSwap
+    KV chunks, one partial per chunk (restricted by kv_lo/kv_hi), merged by the
+    GPU merge with the sink once."""
+    S, H, P = 700, 16, 2
+    prob = synth.make_problem("dense_s8192_h16_p2", S=S, H=H, P=P, device="cuda", seed=9)
+    dev = "cuda"
+    base, rem = divmod(S, 2 * P)
+    bounds, st = [], 0
+    for c in range(2 * P):
+        ln = base + (1 if c < rem else 0)
+        bounds.append((st, st + ln - 1))
+        st += ln
+    C = len(bounds)
+    rows = torch.arange(S, dtype=torch.int32, device=dev).repeat(C)
+    pos = rows.clone()
+    req = torch.zeros_like(rows)
+    lo = torch.tensor([b[0] for b in bounds], dtype=torch.int32, device=dev).repeat_interleave(S)
+    hi = torch.tensor([b[1] for b in bounds], dtype=torch.int32, device=dev).repeat_interleave(S)
+    kv_start = prob.kv_start.to(dev)
+    o_part = torch.empty((C * S, H, 512), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((C * S, H), dtype=torch.float32, device=dev)
+    cpmla.mla_partial_attn_dense(prob.q, kv_start, rows, pos, req, o_part, lse_part,
+                                 softmax_scale=prob.scale, kv=prob.kv, kv_lo=lo, kv_hi=hi)
+    off = torch.arange(0, C * S + 1, C, dtype=torch.int32, device=dev)
+    contrib = (torch.arange(S, dtype=torch.int32, device=dev)[:, None]
+               + S * torch.arange(C, dtype=torch.int32, device=dev)[None, :]).reshape(-1)
+    o = torch.empty((S, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+    cpmla.lse_merge_with_sink(o_part, lse_part, contrib.contiguous(), o, lse, contrib_off=off,
+                              sink=prob.sink)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    # partials of rows whose chunk lies wholly after them are empty
+    assert torch.isneginf(lse_part[S * (C - 1)]).all()
+    ro, rl = pu.oracle_tokens(prob, np.arange(S))
+    pu.compare(o, lse, ro, rl)
+
+
+def test_merge_kernel_against_oracle_merge():
+    rng = np.random.default_rng(17)
+    n_part, H, T = 300, 6, 120
+    op = rng.standard_normal((n_part, H, 512)).astype(np.float32)
+    lp = (rng.standard_normal((n_part, H)) * 3).astype(np.float32)
+    lp[rng.random((n_part, H)) < 0.1] = -np.inf
+    counts = rng.integers(0, 4, T)
+    counts[:3] = [1, 2, 3]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    contrib = rng.integers(0, n_part, off[-1]).astype(np.int32)
+    sink = rng.standard_normal(H).astype(np.float32)
+    for s in (sink, None):
+        ro, rl = orc.merge(op.astype(np.float64), lp.astype(np.float64), off, contrib, sink=s)
+        d = lambda a: torch.from_numpy(a).cuda()
+        o = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        cpmla.lse_merge_with_sink(d(op), d(lp), d(contrib), o, lse, contrib_off=d(off),
+                                  sink=None if s is None else d(s))
+        torch.cuda.synchronize()
+        og = o.float().cpu().numpy()
+        # the partials are unit-scale here, so compare relative to bf16 rounding
+        assert np.abs(og - ro).max() <= 2e-2 * max(1.0, np.abs(ro).max())
+        fin = np.isfinite(rl)
+        lg = lse.cpu().numpy()
+        assert np.array_equal(np.isfinite(lg), fin)
+        assert np.abs(lg[fin] - rl[fin]).max() <= 1e-4 * max(1.0, np.abs(rl[fin]).max())
+        assert (og[counts == 0] == 0).all()
+
+
+def test_repeat_runs_bitwise_identical():
+    prob = synth.make_problem("dense_s8192_h16_p2", S=900, device="cuda", seed=12)
+    o1, l1, _ = pu.run_path(prob)
+    o2, l2, _ = pu.run_path(prob)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+# ----------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("name", ["dense_s8192_h16_p2", "sparse_s32k_h32_p4",
+                                  "sparse_s128k_h16_p2_fp8", "varlen_p8_h64"])
+def test_full_size_workload_sampled_4096_tokens(name):
+    torch.cuda.empty_cache()
+    prob = synth.make_problem(name, device="cuda", seed=0)
+    stats = _check_sample(prob, 4096, seed=1)
+    print(name, stats)
+    del prob
+    torch.cuda.empty_cache()
