@@ -101,9 +101,25 @@ struct Ctrl {
   float inv_l[R];
 };
 
-template <int R>
+// fp8 keeps eight P^T matrices in a region of their own: per 128-dv chunk,
+// P with that chunk's per-key scale folded in, split into a high and a low
+// bf16 part.
+template <int MODE, int R>
+constexpr int p_region_bytes() {
+  return MODE == kSparseFp8 ? 8 * kTileKeys * R * 2 : 0;
+}
+
+template <int MODE, int R>
 constexpr int smem_bytes() {
-  return 1024 /*align slack*/ + R * CPMLA_DQK * 2 + kKb * kKbBytes + (int)sizeof(Ctrl<R>);
+  return 1024 /*align slack*/ + R * CPMLA_DQK * 2 + kKb * kKbBytes + p_region_bytes<MODE, R>() +
+         (int)sizeof(Ctrl<R>);
+}
+
+// Score accumulators: one for bf16 KV; for fp8, one per 128-channel scale
+// group plus one for the rope, so the MMA only ever sees exact E4M3 values.
+template <int MODE>
+constexpr int score_accumulators() {
+  return MODE == kSparseFp8 ? 5 : 1;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -198,13 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int RW = R < 32 ? R : 32;
   constexpr int NSWG = R / RW;
   static_assert(MODE == kDense || NSWG == 1, "sparse kernels use warps 8-11 for the gather");
-  constexpr uint32_t kTmemCols = R * 5 <= 128 ? 128 : (R * 5 <= 256 ? 256 : 512);
+  constexpr int NS = score_accumulators<MODE>();
+  constexpr int kCols = R * (NS + 4);
+  constexpr uint32_t kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
+  static_assert(kCols <= 512, "TMEM budget");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sQ = smem;                       // 9 k-blocks of [R x 64] bf16
   uint8_t *sKV = smem + R * CPMLA_DQK * 2;  // 9 slots of [128 x 64] bf16
-  Ctrl<R> &c = *reinterpret_cast<Ctrl<R> *>(sKV + kKb * kKbBytes);
+  uint8_t *sP = MODE == kSparseFp8 ? sKV + kKb * kKbBytes : sKV + kLatKb * kKbBytes;
+  Ctrl<R> &c = *reinterpret_cast<Ctrl<R> *>(sKV + kKb * kKbBytes + p_region_bytes<MODE, R>());
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -326,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
   const int n_tiles = c.n_tiles;
-  const uint32_t tS = tmem;      // S^T: R columns
-  const uint32_t tO = tmem + R;  // O^T: 4 chunks of R columns
+  const uint32_t tS = tmem;           // S^T: NS accumulators of R columns
+  const uint32_t tO = tmem + NS * R;  // O^T: 4 chunks of R columns
   volatile int *abort = &c.abort;
 
   if (warp == 0) {
@@ -337,7 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t kv_base = smem_u32(sKV);
-      const uint32_t p_base = kv_base + kLatKb * kKbBytes;
+      const uint32_t p_base = smem_u32(sP);
+      constexpr int p_bytes = kTileKeys * PLayout<R>::row_bytes;  // one P^T matrix
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
         const uint32_t par = j & 1;
@@ -348,11 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // fp8: k-blocks 2g, 2g+1 feed accumulator g, the rope feeds 4
+          const uint32_t d_acc = NS == 1 ? tS : tS + (b < kLatKb ? (b >> 1) : 4) * R;
+          const bool first_kb = NS == 1 ? b == 0 : (b == kLatKb || (b & 1) == 0);
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
             const uint64_t da = smem_desc(kv_base + b * kKbBytes + s * 32, 16, 1024, kSwz128);
             const uint64_t db = smem_desc(q_base + b * (R * 128) + s * 32, 16, 1024, kSwz128);
-            mma_bf16_ss(tS, da, db, id_qk, (b | s) != 0 ? 1u : 0u);
+            mma_bf16_ss(d_acc, da, db, id_qk, (first_kb && s == 0) ? 0u : 1u);
           }
         }
         if (!ok) break;
@@ -369,9 +393,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < kTileKeys / 16; ++s) {
             const uint64_t da = smem_desc(kv_base + (2 * ch) * kKbBytes + s * 2048,
                                           kKbBytes /*next 64 dv*/, 1024, kSwz128);
-            const uint64_t db = smem_desc(p_base + s * 16 * PLayout<R>::row_bytes, 8192,
-                                          8 * PLayout<R>::row_bytes, PLayout<R>::swz);
-            mma_bf16_ss(tO + ch * R, da, db, id_pv, (j > 0 || s > 0) ? 1u : 0u);
+#pragma unroll
+            for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
+              const uint32_t pm = p_base + (MODE == kSparseFp8 ? (2 * ch + part) * p_bytes : 0);
+              const uint64_t db = smem_desc(pm + s * 16 * PLayout<R>::row_bytes, 8192,
+                                            8 * PLayout<R>::row_bytes, PLayout<R>::swz);
+              mma_bf16_ss(tO + ch * R, da, db, id_pv, (j > 0 || s > 0 || part > 0) ? 1u : 0u);
+            }
           }
           mma_commit(&c.empty[2 * ch]);
           mma_commit(&c.empty[2 * ch + 1]);
@@ -438,10 +466,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float s[RW];
+      float ksc[4] = {1.f, 1.f, 1.f, 1.f};  // fp8: this key's group scales
+      if (NS == 1) {
 #pragma unroll
-      for (int cc = 0; cc < RW / 16; ++cc)
-        tmem_ld16(tS + lane_off + cbase + cc * 16, s + cc * 16);
-      tmem_ld_wait();
+        for (int cc = 0; cc < RW / 16; ++cc)
+          tmem_ld16(tS + lane_off + cbase + cc * 16, s + cc * 16);
+        tmem_ld_wait();
+      } else {
+        // s = rope part + sum_g scale_g * (q . e4m3 codes of group g)
+        const int64_t src = sparse_key_src(a, row0, j * kTileKeys + t);
+        if (src >= 0) {
+          const float4 sc4 = __ldg(reinterpret_cast<const float4 *>(a.kv_scale) + src);
+          ksc[0] = sc4.x;
+          ksc[1] = sc4.y;
+          ksc[2] = sc4.z;
+          ksc[3] = sc4.w;
+        }
+#pragma unroll
+        for (int cc = 0; cc < RW / 16; ++cc) {
+          tmem_ld16(tS + lane_off + 4 * R + cbase + cc * 16, s + cc * 16);
+          float part[4][16];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) tmem_ld16(tS + lane_off + g * R + cbase + cc * 16, part[g]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            s[cc * 16 + x] += ksc[0] * part[0][x] + ksc[1] * part[1][x] + ksc[2] * part[2][x] +
+                              ksc[3] * part[3][x];
+        }
+      }
       // mask, scale to log2 units
       if (MODE == kDense) {
         const int rel = j * kTileKeys + t;
@@ -479,15 +532,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(bar_id, 128);
       const bool rescale = c.need_rescale[wg] == j + 1;
       // p = 2^(s - m_ref); per-lane partial row sums
+      // (s is overwritten with p)
       uint32_t pk[RW / 2];
 #pragma unroll
       for (int r = 0; r < RW; r += 2) {
         const float m0 = c.m_ref[cbase + r], m1 = c.m_ref[cbase + r + 1];
         const float p0 = fast_exp2(s[r] - (m0 == -INFINITY ? 0.f : m0));
         const float p1 = fast_exp2(s[r + 1] - (m1 == -INFINITY ? 0.f : m1));
+        if (NS == 1) pk[r / 2] = pack_bf16x2(p0, p1);
         l_part[r] = l_part[r] * c.alpha[cbase + r] + p0;
         l_part[r + 1] = l_part[r + 1] * c.alpha[cbase + r + 1] + p1;
-        pk[r / 2] = pack_bf16x2(p0, p1);
+        s[r] = p0;
+        s[r + 1] = p1;
       }
       if (rescale) {
         // O^T columns *= alpha; PV(j-1) is complete (QK(j) was issued after it)
@@ -508,13 +564,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // this warpgroup's part of P^T row t, into the rope slot (the score
       // GEMM of tile j has consumed it)
-      uint8_t *prow = sKV + kLatKb * kKbBytes + t * PLayout<R>::row_bytes;
 #pragma unroll
-      for (int ch = 0; ch < RW / 8; ++ch) {
-        const int logical = wg * (RW / 8) + ch;
-        const int phys = logical ^ PLayout<R>::chunk_xor(t);
-        *reinterpret_cast<uint4 *>(prow + phys * 16) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      for (int m = 0; m < (NS == 1 ? 1 : 8); ++m) {
+        uint8_t *prow = sP + m * (kTileKeys * PLayout<R>::row_bytes) + t * PLayout<R>::row_bytes;
+        if (NS != 1) {
+          // P^T of dv chunk m/2: p times this key's scale of channel group m/2,
+          // as a high bf16 part (m even) and the bf16 rounding of the rest (m
+          // odd); the PV GEMM adds both, so P reaches the tensor core with ~16
+          // significant bits
+#pragma unroll
+          for (int r = 0; r < RW; r += 2) {
+            const float x0 = s[r] * ksc[m >> 1], x1 = s[r + 1] * ksc[m >> 1];
+            const uint32_t hi = pack_bf16x2(x0, x1);
+            pk[r / 2] = (m & 1) ? pack_bf16x2(x0 - __uint_as_float(hi << 16),
+                                              x1 - __uint_as_float(hi & 0xFFFF0000u))
+                                : hi;
+          }
+        }
+#pragma unroll
+        for (int ch = 0; ch < RW / 8; ++ch) {
+          const int logical = wg * (RW / 8) + ch;
+          const int phys = logical ^ PLayout<R>::chunk_xor(t);
+          *reinterpret_cast<uint4 *>(prow + phys * 16) =
+              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -610,20 +683,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               gp = a.kv_rope + (src >= 0 ? src : 0) * CPMLA_DROPE + cc * 8;
             cp_async_16(dst, gp, src >= 0 ? 16u : 0u);
           } else {
-            // fp8 latent: 8 codes -> 8 bf16, times the 128-channel group scale
+            // fp8 latent: 8 codes -> 8 bf16, exactly (every E4M3 value is a
+            // bf16 value); the group scales are applied to the scores and to
+            // P^T instead
             uint4 outv = make_uint4(0, 0, 0, 0);
             if (src >= 0) {
               const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
                   a.kv8 + src * CPMLA_DV + b * kKbDims + cc * 8));
-              const float sc = __ldg(a.kv_scale + src * (CPMLA_DV / 128) + (b >> 1));
               const float2 f0 = e4m3x2_to_float2((uint16_t)(raw.x & 0xFFFFu));
               const float2 f1 = e4m3x2_to_float2((uint16_t)(raw.x >> 16));
               const float2 f2 = e4m3x2_to_float2((uint16_t)(raw.y & 0xFFFFu));
               const float2 f3 = e4m3x2_to_float2((uint16_t)(raw.y >> 16));
-              outv = make_uint4(pack_bf16x2(f0.x * sc, f0.y * sc),
-                                pack_bf16x2(f1.x * sc, f1.y * sc),
-                                pack_bf16x2(f2.x * sc, f2.y * sc),
-                                pack_bf16x2(f3.x * sc, f3.y * sc));
+              outv = make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
+                                pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y));
             }
             *reinterpret_cast<uint4 *>(dst) = outv;
           }
@@ -675,7 +747,7 @@ EncodeTiledFn encode_fn() {
 
 template <int MODE, int R>
 int launch(const AttnArgs &args, const CUtensorMap &tm, int n_items, cudaStream_t stream) {
-  constexpr int smem = smem_bytes<R>();
+  constexpr int smem = smem_bytes<MODE, R>();
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = mla_attn_kernel<MODE, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -718,8 +790,9 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   } else {
     CPMLA_CHECK_ARG(kv_fp8 && kv_scale && kv_rope, "%s: fp8 KV needs kv_fp8, kv_scale, kv_rope",
                     fn);
-    CPMLA_CHECK_ARG(((uintptr_t)kv_fp8 & 15) == 0 && ((uintptr_t)kv_rope & 15) == 0,
-                    "%s: kv_fp8 and kv_rope must be 16-byte aligned", fn);
+    CPMLA_CHECK_ARG(((uintptr_t)kv_fp8 & 15) == 0 && ((uintptr_t)kv_rope & 15) == 0 &&
+                        ((uintptr_t)kv_scale & 15) == 0,
+                    "%s: kv_fp8, kv_scale and kv_rope must be 16-byte aligned", fn);
   }
   if (sparse) CPMLA_CHECK_ARG(topk != nullptr, "%s: topk_idx is NULL", fn);
   int *status = status_word();
@@ -756,9 +829,12 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
     args.g = 64 / args.hc;
     R = 64;
   } else {
-    args.hc = H <= 32 ? H : 32;
-    if (H > 32 && H % 32 != 0)
-      return fail(CPMLA_ERR_UNSUPPORTED, "%s: H=%d > 32 must be a multiple of 32", fn, H);
+    // fp8 works on 16 heads at a time (its split-P region is sized for R = 16)
+    const int hmax = kv_format == CPMLA_KV_FP8_E4M3_G128 ? 16 : 32;
+    args.hc = H <= hmax ? H : hmax;
+    if (H > hmax && H % hmax != 0)
+      return fail(CPMLA_ERR_UNSUPPORTED, "%s: H=%d > %d must be a multiple of %d", fn, H, hmax,
+                  hmax);
     args.g = 1;
     R = args.hc <= 16 ? 16 : 32;
   }
@@ -787,8 +863,7 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   if (kv_format == CPMLA_KV_BF16)
     return R == 16 ? launch<kSparseBf16, 16>(args, tm, (int)n_items, st)
                    : launch<kSparseBf16, 32>(args, tm, (int)n_items, st);
-  return R == 16 ? launch<kSparseFp8, 16>(args, tm, (int)n_items, st)
-                 : launch<kSparseFp8, 32>(args, tm, (int)n_items, st);
+  return launch<kSparseFp8, 16>(args, tm, (int)n_items, st);
 }
 
 }  // namespace

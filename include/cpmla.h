@@ -134,7 +134,8 @@ int pcp_dualchunk_partition(int P, int B, const int32_t *cu_seqlens, const int32
  *   q_token_stride  elements between tokens, >= H*576, multiple of 8 (host)
  *   H            heads, 1..128; if H > 64 it must be a multiple of 64 (host)
  *   kv_format    CPMLA_KV_* (host).  Dense accepts CPMLA_KV_BF16 only.
- *   kv / kv_fp8, kv_scale, kv_rope   per kv_format (unused ones may be NULL)
+ *   kv / kv_fp8, kv_scale, kv_rope   per kv_format (unused ones may be NULL);
+ *                each 16-byte aligned
  *   s_kv         KV rows (host); every key read lies in [0, s_kv)
  *   kv_start     int64 [B] KV row of request b's position 0
  *   rows, pos, req  int32 [n_rows] as produced by pcp_dualchunk_partition
