@@ -310,7 +310,8 @@ def main():
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16"], 4), "traffic": None,
-                     "kernel": "mla_attn_kernel", "peak_source": pk["source"] + " burst bf16"},
+                     "kernel": "mla_sparse_kernel" if prob.topk else "mla_dense_kernel",
+                     "peak_source": pk["source"] + " burst bf16"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm"],
                            "unit": "GB/s", "frac": round(merge_gbs / pk["hbm"], 4),
                            "bytes": merge_bytes},

@@ -1,0 +1,144 @@
+// attn_common.cuh -- pieces shared by the dense and the sparse partial-attention
+// kernels: work-item arguments, the P^T shared-memory layout, warp
+// transpose-reductions, conversions and the elected bounded wait.
+//
+// Both kernels compute, for each shard row (token g at position t) and head h,
+// the partial attention of "[DeepSeekV4][PCP] Enable context-parallel prefill
+// for hybrid KV and MegaMoE", "Implementation summary": O and LSE over the
+// row's keys, no sink.  Scores use the 576-wide absorbed latent+rope key;
+// values are the 512-wide latent ("[Core] Add MRV2 virtual-batch PCP for MLA",
+// "DualChunkSwap partitioning": every shard reads the full latent KV).
+#pragma once
+
+#include "cpmla_internal.cuh"
+
+namespace cpmla {
+
+
+constexpr int kTileKeys = 128;                     // keys per KV tile (MMA M)
+constexpr int kKbDims = 64;                        // dims per k-block (128 B rows)
+constexpr int kLatKb = CPMLA_DV / kKbDims;         // 8 latent k-blocks
+constexpr int kKb = CPMLA_DQK / kKbDims;           // 9 k-blocks incl. rope
+constexpr int kKbBytes = kTileKeys * kKbDims * 2;  // 16 KB
+constexpr int kThreads = 384;
+constexpr int kSoftmaxWarp0 = 4;
+
+enum Mode { kDense = 0, kSparseBf16 = 1, kSparseFp8 = 2 };
+
+struct AttnArgs {
+  const __nv_bfloat16 *q;
+  int64_t q_stride;  // elements between tokens
+  int H;
+  const __nv_bfloat16 *kv;
+  const uint8_t *kv8;
+  const float *kv_scale;
+  const __nv_bfloat16 *kv_rope;
+  int64_t s_kv;
+  const int64_t *kv_start;
+  const int32_t *rows;
+  const int32_t *pos;
+  const int32_t *req;
+  int n_rows;
+  const int32_t *kv_lo;
+  const int32_t *kv_hi;
+  const int32_t *topk;
+  int k;
+  float scale_log2;  // softmax scale * log2(e)
+  float *o_part;
+  float *lse_part;
+  int hc;         // heads per CTA
+  int g;          // tokens per CTA
+  int n_hgroups;  // H / hc
+  int *status;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// P^T layout for the PV GEMM's B operand: MN-major, N = R rows per key row,
+// swizzle width = R*2 bytes (16 rows: 32 B, 32: 64 B, 64: 128 B).
+template <int R>
+struct PLayout {
+  static constexpr uint32_t swz = R == 64 ? kSwz128 : (R == 32 ? kSwz64 : kSwz32);
+  static constexpr int row_bytes = R * 2;
+  __device__ static __forceinline__ int chunk_xor(int key) {
+    return R == 64 ? (key & 7) : (R == 32 ? ((key >> 1) & 3) : ((key >> 2) & 1));
+  }
+};
+
+// Transpose-reduction of N per-lane values across the 32 lanes of a warp
+// (N = 32: afterwards lane l holds row l in v[0]; N = 16: lane l holds row
+// l/2).  Each step trades half of the values with the partner lane, so it
+// takes N-1 shuffles instead of 5N.
+template <int N, bool kMax>
+__device__ __forceinline__ void warp_transpose_reduce(float *v, int lane) {
+  int n = N;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (n > 1) {
+      const bool upper = (lane & off) != 0;
+      const int h = n >> 1;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < h) {
+          const float mine = upper ? v[h + i] : v[i];
+          const float give = upper ? v[i] : v[h + i];
+          const float got = __shfl_xor_sync(0xffffffffu, give, off);
+          v[i] = kMax ? fmaxf(mine, got) : mine + got;
+        }
+      }
+      n = h;
+    } else {
+      const float got = __shfl_xor_sync(0xffffffffu, v[0], off);
+      v[0] = kMax ? fmaxf(v[0], got) : v[0] + got;
+    }
+  }
+}
+
+// e4m3 pair -> two floats (exact), low byte first.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  __half2 hh = *reinterpret_cast<__half2 *>(&h2);
+  return __half22float2(hh);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// Global KV row of entry e of shard row `row`'s top-k list, or -1 when the
+// entry is empty, outside the row's causal prefix or KV, or outside its
+// optional [kv_lo, kv_hi] restriction.
+__device__ __forceinline__ int64_t sparse_key_src(const AttnArgs &a, int row, int e) {
+  if (e >= a.k) return -1;
+  const int p = a.topk[(int64_t)a.rows[row] * a.k + e];
+  const int tpos = a.pos[row];
+  if (p < 0 || p > tpos) return -1;
+  if (a.kv_lo && p < a.kv_lo[row]) return -1;
+  if (a.kv_hi && p > a.kv_hi[row]) return -1;
+  const int64_t src = a.kv_start[a.req[row]] + p;
+  return src < a.s_kv ? src : -1;
+}
+
+// Elected bounded wait whose result every thread of a named-barrier group
+// sees (so no thread skips a barrier the others enter).
+__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, int t, int bar_id,
+                                           int *flag_pair, int &seq, volatile int *abort,
+                                           int *status) {
+  int *f = flag_pair + (seq & 1);
+  ++seq;
+  if (t == 0) *f = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  named_bar_sync(bar_id, 128);
+  return *reinterpret_cast<volatile int *>(f) != 0;
+}
+
+// Launchers (one per translation unit); n_items CTAs, one work item each.
+int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st);
+int launch_sparse(int mode, int R, const AttnArgs &args, int n_items, cudaStream_t st);
+
+}  // namespace cpmla

@@ -1,0 +1,496 @@
+// attn_dense.cu -- dense-causal partial MLA attention (output + LSE, no sink)
+// for context-parallel prefill, bf16 latent KV, on sm_103a.
+//
+// "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
+// MegaMoE", "Implementation summary": per-shard partial attention merged
+// later by LSE; "[Core] Add MRV2 virtual-batch PCP for MLA", "DualChunkSwap
+// partitioning": each shard's rows attend causally over the full latent KV.
+//
+// One CTA = 64 query rows (G tokens x Hc heads of consecutive shard rows).
+//   * Score GEMM key-major: S^T = K . Q^T, M = 128 keys, N = 64 rows, K = 576,
+//     into one of two TMEM buffers, so the score GEMM of tile j+1 runs while
+//     the softmax of tile j does.  PV GEMM: O^T += V^T . P^T, M = 128 dv x 4
+//     chunks, N = 64, K = 128 keys; O^T stays in TMEM (256 columns).
+//   * One ring of four 32 KB slots streams everything the tensor core reads,
+//     in the order it reads it: K of a tile as five slots (k-block pairs of
+//     [128 keys x 64 dims], the rope k-block alone) and V of a tile as four
+//     128-dv chunks [128 keys x 128 dv] -- a second read of the same
+//     L2-resident rows, so neither GEMM holds shared memory the other needs,
+//     and all 128 KB of the ring are in flight whatever the tensor core is
+//     doing.  One producer thread fills it with TMA (128-byte swizzle).
+//   * Warp 0 issues every tcgen05.mma from one thread in the order
+//     QK(0), QK(1), PV(0), QK(2), PV(1), ...; warp 1 is the producer; warps
+//     4-11 are two softmax warpgroups of 32 rows each (thread i = TMEM lane
+//     i = key i of a tile / dv i of an O^T chunk).
+//   * Tiles that lie inside every row's causal range skip the mask.
+//   * Every wait is bounded; on expiry the CTA records CPMLA_ERR_TIMEOUT,
+//     drains its copies and MMAs, and exits.
+#include <cmath>
+
+#include "attn_common.cuh"
+
+namespace cpmla {
+namespace {
+
+constexpr int kR = 64;                      // query rows per CTA (MMA N)
+constexpr int kRW = 32;                     // rows per softmax warpgroup
+constexpr int kNS = 4;                      // ring slots
+constexpr int kSlotBytes = 2 * kKbBytes;    // 32 KB: two k-blocks or one 128-dv chunk
+constexpr int kKPairs = 5;                  // K of a tile: k-block pairs 0-3 + rope
+constexpr int kVChunks = 4;                 // V of a tile: 128-dv chunks
+constexpr int kPBytes = kTileKeys * kR * 2; // P^T, 16 KB
+constexpr uint32_t kTmemCols = 512;         // S^T x2 (128) + O^T (256)
+
+struct DenseCtrl {
+  uint64_t full[kNS];
+  uint64_t empty[kNS];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t p_free;
+  uint64_t o_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int n_tiles;
+  int open_lo, open_hi;  // tiles j in [open_lo, open_hi) need no mask
+  int bflag[2][2];
+  int need_rescale[2];
+  int64_t tile_lo;  // global KV row of key 0 of tile 0
+  int rlo[kR];      // per row: valid keys relative to tile_lo, inclusive
+  int rhi[kR];
+  float red[2][4][32];
+  float m_ref[kR];
+  float alpha[kR];
+  float lse[kR];
+  float inv_l[kR];
+};
+
+constexpr int kQBytes = kR * CPMLA_DQK * 2;
+constexpr int kSmem = 1024 + kQBytes + kPBytes + kNS * kSlotBytes + (int)sizeof(DenseCtrl);
+static_assert(kSmem <= 232448, "shared memory budget");
+
+// Bounded wait that ignores the abort flag (used to drain own copies).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+// Valid key range of shard row i, as global KV rows (inclusive), or lo > hi.
+__device__ __forceinline__ void row_range(const AttnArgs &a, int i, int64_t &lo, int64_t &hi) {
+  const int64_t base = a.kv_start[a.req[i]];
+  lo = 0;
+  hi = a.pos[i];
+  if (a.kv_lo) lo = lo > a.kv_lo[i] ? lo : a.kv_lo[i];
+  if (a.kv_hi) hi = hi < a.kv_hi[i] ? hi : a.kv_hi[i];
+  lo += base;
+  hi += base;
+  if (hi > a.s_kv - 1) hi = a.s_kv - 1;
+  if (lo < 0) lo = 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_dense_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sQ = smem;                      // 9 k-blocks of [64 rows x 64 dims]
+  uint8_t *sP = sQ + kQBytes;              // P^T [128 keys x 64 rows]
+  uint8_t *sRing = sP + kPBytes;           // kNS slots of 32 KB
+  DenseCtrl &c = *reinterpret_cast<DenseCtrl *>(sRing + kNS * kSlotBytes);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  // reversed item order: the last shard rows of a request (longest causal
+  // ranges) start first, the shortest finish the grid
+  const int item = gridDim.x - 1 - blockIdx.x;
+  const int row_group = item / a.n_hgroups;
+  const int hg = item - row_group * a.n_hgroups;
+  const int row0 = row_group * a.g;
+  const int h0 = hg * a.hc;
+  const int r_valid = a.g * a.hc;
+
+  // ------------------------------------------------------------ setup
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&c.s_full[s], 1);
+      mbar_init(&c.s_free[s], 2 * 128);
+    }
+    mbar_init(&c.p_full, 2 * 128);
+    mbar_init(&c.p_free, 1);
+    mbar_init(&c.o_full, 1);
+    mbar_init(&c.drain, 1);
+    c.abort = 0;
+    c.need_rescale[0] = c.need_rescale[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
+  if (warp == 1 && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (tid < kR) {
+    c.m_ref[tid] = -INFINITY;
+    c.alpha[tid] = 1.f;
+  }
+  // Q rows -> K-major, 128-byte-swizzled k-blocks (zero rows for padding)
+  for (int idx = tid; idx < kR * (CPMLA_DQK / 8); idx += kThreads) {
+    const int r = idx / (CPMLA_DQK / 8);
+    const int ch = idx - r * (CPMLA_DQK / 8);
+    const int l = r / a.hc, hh = r - l * a.hc;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < r_valid && row0 + l < a.n_rows) {
+      const int64_t gtok = a.rows[row0 + l];
+      v = __ldg(reinterpret_cast<const uint4 *>(a.q + gtok * a.q_stride +
+                                                (int64_t)(h0 + hh) * CPMLA_DQK) +
+                ch);
+    }
+    const int kb = ch >> 3, cc = ch & 7;
+    *reinterpret_cast<uint4 *>(sQ + kb * (kR * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+  }
+  // key range of the item and the tiles that need no mask
+  if (tid == 0) {
+    int64_t lo_min = INT64_MAX, hi_max = INT64_MIN, lo_max = INT64_MIN, hi_min = INT64_MAX;
+    for (int l = 0; l < a.g && row0 + l < a.n_rows; ++l) {
+      int64_t lo, hi;
+      row_range(a, row0 + l, lo, hi);
+      if (a.pos[row0 + l] + a.kv_start[a.req[row0 + l]] > a.s_kv - 1)
+        record_status(a.status, CPMLA_ERR_INDEX);
+      lo_max = lo > lo_max ? lo : lo_max;
+      hi_min = hi < hi_min ? hi : hi_min;
+      if (hi >= lo) {
+        lo_min = lo < lo_min ? lo : lo_min;
+        hi_max = hi > hi_max ? hi : hi_max;
+      }
+    }
+    if (hi_max < lo_min) {
+      c.n_tiles = 0;
+      c.tile_lo = 0;
+      c.open_lo = c.open_hi = 0;
+    } else {
+      c.n_tiles = (int)((hi_max - lo_min + kTileKeys) / kTileKeys);
+      c.tile_lo = lo_min;
+      // tile j is open for every row when 128j >= lo_max - tile_lo and
+      // 128j + 127 <= hi_min - tile_lo
+      const int64_t a_lo = lo_max - lo_min, a_hi = hi_min - lo_min;
+      c.open_lo = (int)((a_lo + kTileKeys - 1) / kTileKeys);
+      c.open_hi = a_hi < 0 ? 0 : (int)((a_hi + 1) / kTileKeys);
+    }
+  }
+  __syncthreads();
+  if (tid < kR) {
+    const int l = tid / a.hc;
+    int rlo = 1, rhi = 0;  // empty
+    if (tid < r_valid && row0 + l < a.n_rows) {
+      int64_t lo, hi;
+      row_range(a, row0 + l, lo, hi);
+      if (hi >= lo) {
+        rlo = (int)(lo - c.tile_lo);
+        rhi = (int)(hi - c.tile_lo);
+      }
+    }
+    c.rlo[tid] = rlo;
+    c.rhi[tid] = rhi;
+  }
+  fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  const int n_tiles = c.n_tiles;
+  const uint32_t tO = tmem + 2 * kR;  // O^T chunk c at tO + c*64; S^T buffer b at tmem + b*64
+  volatile int *abort = &c.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(128, kR, 0, 0);
+      constexpr uint32_t id_pv = idesc_bf16(128, kR, 1, 1);
+      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
+      const uint32_t ring = smem_u32(sRing);
+      uint32_t n = 0;  // ring items consumed so far
+      bool ok = true;
+      for (int i = 0; i <= n_tiles && ok; ++i) {
+        if (i < n_tiles) {
+          const int sb = i & 1;
+          if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dS = tmem + sb * kR;
+          for (int pr = 0; pr < kKPairs; ++pr, ++n) {
+            const uint32_t slot = n % kNS;
+            if (!mbar_wait(&c.full[slot], (n / kNS) & 1, abort, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int nkb = pr < 4 ? 2 : 1;
+            for (int h = 0; h < nkb; ++h) {
+              const int b = 2 * pr + h;  // k-block (8 = rope)
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const uint64_t da =
+                    smem_desc(ring + slot * kSlotBytes + h * kKbBytes + s * 32, 16, 1024, kSwz128);
+                const uint64_t db = smem_desc(q_base + b * (kR * 128) + s * 32, 16, 1024, kSwz128);
+                mma_bf16_ss(dS, da, db, id_qk, (b | s) != 0 ? 1u : 0u);
+              }
+            }
+            mma_commit(&c.empty[slot]);
+          }
+          if (!ok) break;
+          mma_commit(&c.s_full[sb]);
+        }
+        if (i >= 1) {
+          const int j = i - 1;
+          if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int ch = 0; ch < kVChunks; ++ch, ++n) {
+            const uint32_t slot = n % kNS;
+            if (!mbar_wait(&c.full[slot], (n / kNS) & 1, abort, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < kTileKeys / 16; ++s) {
+              const uint64_t da = smem_desc(ring + slot * kSlotBytes + s * 2048, kKbBytes, 1024,
+                                            kSwz128);
+              const uint64_t db = smem_desc(p_base + s * 2048, 8192, 1024, kSwz128);
+              mma_bf16_ss(tO + ch * kR, da, db, id_pv, (j > 0 || s > 0) ? 1u : 0u);
+            }
+            mma_commit(&c.empty[slot]);
+          }
+          if (!ok) break;
+          mma_commit(&c.p_free);
+        }
+      }
+      mma_commit(&c.o_full);
+      if (!ok) {
+        mma_commit(&c.drain);
+        drain_wait(&c.drain, 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------- producer
+    // the same item order as the MMA issuer: K(0), then per i >= 1
+    // K(i) (if any) followed by V(i-1)
+    if (lane == 0) {
+      uint32_t n = 0;
+      bool ok = true;
+      for (int i = 0; i <= n_tiles && ok; ++i) {
+        for (int part = 0; part < 2 && ok; ++part) {
+          const bool is_k = part == 0;
+          if (is_k ? i >= n_tiles : i == 0) continue;
+          const int tile = is_k ? i : i - 1;
+          const int y = (int)(c.tile_lo + (int64_t)tile * kTileKeys);
+          const int items = is_k ? kKPairs : kVChunks;
+          for (int it = 0; it < items; ++it, ++n) {
+            const uint32_t slot = n % kNS;
+            if (n >= (uint32_t)kNS &&
+                !mbar_wait(&c.empty[slot], ((n / kNS) - 1) & 1, abort, a.status)) {
+              ok = false;
+              break;
+            }
+            uint8_t *dst = sRing + slot * kSlotBytes;
+            // K pair it: dims [128 it, 128 it + 128) (the rope pair has one
+            // k-block); V chunk it: dv [128 it, 128 it + 128) -- the same boxes
+            const int nkb = (is_k && it == kKPairs - 1) ? 1 : 2;
+            mbar_arrive_expect_tx(&c.full[slot], nkb * kKbBytes);
+            tma_load_2d(dst, &tm_kv, it * 128, y, &c.full[slot]);
+            if (nkb == 2) tma_load_2d(dst + kKbBytes, &tm_kv, it * 128 + 64, y, &c.full[slot]);
+          }
+        }
+      }
+      if (!ok) {
+        // wait for the last load issued into each slot
+        for (uint32_t s2 = 0; s2 < (uint32_t)kNS; ++s2) {
+          if (n <= s2) continue;
+          const uint32_t last = n - 1 - ((n - 1 - s2) % kNS);
+          drain_wait(&c.full[s2], (last / kNS) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kSoftmaxWarp0) {
+    // ---------------------------------------------------- softmax + epilogue
+    const int wg = (warp - kSoftmaxWarp0) >> 2;
+    const int t = tid - kSoftmaxWarp0 * 32 - wg * 128;
+    const int q4 = (warp - kSoftmaxWarp0) & 3;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int cbase = wg * kRW;
+    const int bar_id = 1 + wg;
+    const int open_lo = c.open_lo, open_hi = c.open_hi;
+    int seq = 0;
+    float l_part[kRW];
+#pragma unroll
+    for (int r = 0; r < kRW; ++r) l_part[r] = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      if (!group_wait(&c.s_full[sb], (j >> 1) & 1, t, bar_id, c.bflag[wg], seq, abort,
+                      a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kRW];
+      tmem_ld16(tmem + sb * kR + lane_off + cbase, s);
+      tmem_ld16(tmem + sb * kR + lane_off + cbase + 16, s + 16);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&c.s_free[sb]);  // the next-but-one score GEMM may overwrite it
+      if (j >= open_lo && j < open_hi) {
+#pragma unroll
+        for (int r = 0; r < kRW; ++r) s[r] *= a.scale_log2;
+      } else {
+        const int rel = j * kTileKeys + t;
+#pragma unroll
+        for (int r = 0; r < kRW; ++r) {
+          const bool valid = rel >= c.rlo[cbase + r] && rel <= c.rhi[cbase + r];
+          s[r] = valid ? s[r] * a.scale_log2 : -INFINITY;
+        }
+      }
+      {
+        float v[kRW];
+#pragma unroll
+        for (int r = 0; r < kRW; ++r) v[r] = s[r];
+        warp_transpose_reduce<kRW, true>(v, lane);
+        c.red[wg][q4][lane] = v[0];
+      }
+      named_bar_sync(bar_id, 128);
+      if (t < kRW) {
+        const int r = cbase + t;
+        const float tile_max = fmaxf(fmaxf(c.red[wg][0][t], c.red[wg][1][t]),
+                                     fmaxf(c.red[wg][2][t], c.red[wg][3][t]));
+        const float m_old = c.m_ref[r];
+        float m_new = m_old;
+        if (tile_max > m_old + 8.f) m_new = tile_max;  // lazy move of the reference
+        c.alpha[r] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
+        c.m_ref[r] = m_new;
+        if (j > 0 && m_new != m_old) c.need_rescale[wg] = j + 1;
+      }
+      named_bar_sync(bar_id, 128);
+      const bool rescale = c.need_rescale[wg] == j + 1;
+      uint32_t pk[kRW / 2];
+#pragma unroll
+      for (int r = 0; r < kRW; r += 2) {
+        const float m0 = c.m_ref[cbase + r], m1 = c.m_ref[cbase + r + 1];
+        const float p0 = fast_exp2(s[r] - (m0 == -INFINITY ? 0.f : m0));
+        const float p1 = fast_exp2(s[r + 1] - (m1 == -INFINITY ? 0.f : m1));
+        l_part[r] = l_part[r] * c.alpha[cbase + r] + p0;
+        l_part[r + 1] = l_part[r + 1] * c.alpha[cbase + r + 1] + p1;
+        pk[r / 2] = pack_bf16x2(p0, p1);
+      }
+      // PV(j-1) must be done before P^T is overwritten or O^T rescaled
+      if (j >= 1 && !group_wait(&c.p_free, (j - 1) & 1, t, bar_id, c.bflag[wg], seq, abort,
+                                a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (rescale) {
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+          for (int cc = 0; cc < kRW / 16; ++cc) {
+            float o[16];
+            const uint32_t col = tO + lane_off + ch * kR + cbase + cc * 16;
+            tmem_ld16(col, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) o[x] *= c.alpha[cbase + cc * 16 + x];
+            tmem_st16(col, o);
+          }
+        }
+        tmem_st_wait();
+      }
+      uint8_t *prow = sP + t * 128;
+#pragma unroll
+      for (int ch = 0; ch < kRW / 8; ++ch) {
+        const int phys = (wg * (kRW / 8) + ch) ^ (t & 7);
+        *reinterpret_cast<uint4 *>(prow + phys * 16) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&c.p_full);
+    }
+    // ------------------------------------------------ epilogue
+    if (ok) ok = group_wait(&c.o_full, 0, t, bar_id, c.bflag[wg], seq, abort, a.status);
+    if (ok) {
+      tc_fence_after();
+      warp_transpose_reduce<kRW, false>(l_part, lane);
+      c.red[wg][q4][lane] = l_part[0];
+      named_bar_sync(bar_id, 128);
+      if (t < kRW) {
+        const int r = cbase + t;
+        const float l = c.red[wg][0][t] + c.red[wg][1][t] + c.red[wg][2][t] + c.red[wg][3][t];
+        const float m = c.m_ref[r];
+        const bool empty = !(l > 0.f) || m == -INFINITY;
+        c.lse[r] = empty ? -INFINITY : (m + __log2f(l)) * 0.69314718055994530942f;
+        c.inv_l[r] = empty ? 0.f : 1.f / l;
+        if (r < r_valid) {
+          const int lrow = r / a.hc, hh = r - lrow * a.hc;
+          const int i = row0 + lrow;
+          if (i < a.n_rows) a.lse_part[(int64_t)i * a.H + h0 + hh] = c.lse[r];
+        }
+      }
+      named_bar_sync(bar_id, 128);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int cc = 0; cc < kRW / 16; ++cc) {
+          float o[16];
+          if (n_tiles > 0) {
+            tmem_ld16(tO + lane_off + ch * kR + cbase + cc * 16, o);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) o[x] = 0.f;
+          }
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const int r = cbase + cc * 16 + x;
+            if (r < r_valid) {
+              const int lrow = r / a.hc, hh = r - lrow * a.hc;
+              const int i = row0 + lrow;
+              if (i < a.n_rows)
+                a.o_part[((int64_t)i * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
+                    o[x] * c.inv_l[r];
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st) {
+  cudaError_t e =
+      cudaFuncSetAttribute(mla_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return cuda_fail(e, "dense attention: set shared memory size");
+  mla_dense_kernel<<<n_items, kThreads, kSmem, st>>>(args, tm_kv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "dense attention: launch");
+  return CPMLA_OK;
+}
+
+}  // namespace cpmla
