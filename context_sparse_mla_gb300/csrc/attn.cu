@@ -121,25 +121,30 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   const int64_t n_items = n_groups * args.n_hgroups;
   CPMLA_CHECK_ARG(n_items <= INT32_MAX, "%s: too many work items", fn);
 
-  CUtensorMap tm;
-  memset(&tm, 0, sizeof tm);
-  if (!sparse) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return fail(CPMLA_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
-    cuuint64_t dims[2] = {(cuuint64_t)CPMLA_DQK, (cuuint64_t)s_kv};
-    cuuint64_t strides[1] = {(cuuint64_t)CPMLA_DQK * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kKbDims, (cuuint32_t)kTileKeys};
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(CPMLA_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
+  // 2D map over a row-major [s_kv, width] array, box [box_w x box_h]
+  auto encode = [&](CUtensorMap *tm, CUtensorMapDataType dt, const void *base, int width,
+                    int elem_bytes, int box_w, int box_h, CUtensorMapSwizzle swz) {
+    memset(tm, 0, sizeof *tm);
+    cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)s_kv};
+    cuuint64_t strides[1] = {(cuuint64_t)width * elem_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)box_w, (cuuint32_t)box_h};
     cuuint32_t estr[2] = {1, 1};
-    CUresult cr = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kv), dims,
-                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS) return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr);
-  }
+    return enc(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!sparse) return launch_dense(args, tm, (int)n_items, st);
-  return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args,
-                       (int)n_items, st);
+  if (sparse)
+    return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args,
+                         (int)n_items, st);
+  // 128-key x 64-dim tiles of the bf16 KV
+  CUtensorMap tm;
+  const CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, CPMLA_DQK, 2, kKbDims,
+                             kTileKeys, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (cr != CUDA_SUCCESS) return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr);
+  return launch_dense(args, tm, (int)n_items, st);
 }
 
 }  // namespace

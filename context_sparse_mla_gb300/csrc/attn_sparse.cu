@@ -3,23 +3,34 @@
 //
 // "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
 // MegaMoE", "Implementation summary": per-shard partial attention over each
-// query's own top-k keys; "[Feature][PCP] Add DeepSeek-V4.1-Flash support",
-// "Supported Scope": the sparse MLA path with an fp8 KV cache.
+// query's own top-k keys, merged later by LSE; "[Feature][PCP] Add
+// DeepSeek-V4.1-Flash support", "Supported Scope": the sparse MLA path with an
+// fp8 KV cache.
 //
 // One CTA = one token x up to 32 heads (16 for fp8): its keys are its own, so
-// a KV tile serves only that token's heads.
-//   * Warps 8-11 gather the token's keys, 128 per tile, into nine 16 KB
-//     k-blocks [128 keys x 64 dims], 128-byte swizzled: cp.async for bf16;
-//     for fp8, load + exact E4M3 -> bf16 conversion + store (the per-128-
-//     channel scales are applied later, so the MMA sees exact values).
-//   * Warp 0 issues tcgen05.mma from one thread: S^T = K . Q^T (M = 128 keys,
-//     N = R rows, K = 576; fp8 keeps one fp32 accumulator per channel group
-//     and one for the rope), then O^T += V^T . P^T (M = 128 dv x 4 chunks,
-//     N = R, K = 128 keys).  TMEM holds S^T and O^T.
-//   * Warps 4-7 (thread i = key i / dv i of TMEM lane i) apply the scales,
-//     mask, run the online softmax with a lazily moved base-2 reference, write
-//     P^T (fp8: per chunk, with that chunk's scale, split into high and low
-//     bf16 parts) and finally normalise and store O and LSE.
+// a KV tile serves only that token's heads.  The pipeline is the dense
+// kernel's, fed by a gather instead of TMA:
+//   * Score GEMM key-major: S^T = K . Q^T, M = 128 keys, N = R rows, K = 576,
+//     into one of two TMEM buffers, so the score GEMM of tile j+1 overlaps the
+//     softmax of tile j.  fp8 keeps one fp32 accumulator per 128-channel scale
+//     group and one for the rope, so the MMA only sees exact E4M3 values.  PV
+//     GEMM: O^T += V^T . P^T, M = 128 dv x 4 chunks, N = R, K = 128 keys.
+//   * One ring of 32 KB slots carries what the tensor core reads, in the order
+//     it reads it: K of a tile as five items (128-dim pairs of k-blocks
+//     [128 keys x 64 dims], the rope alone) and V of the previous tile as four
+//     128-dv chunks, gathered again (the same bytes as K pairs 0-3).
+//   * Warps 8-11 gather: once per tile they resolve the 128 keys' KV rows
+//     (and fp8 scales) into shared memory for everyone, then issue each item
+//     with cp.async by all 128 threads, whose completion arrives on the item's
+//     barrier by itself (cp.async.mbarrier.arrive.noinc), so the gather runs
+//     as far ahead as the ring allows.  fp8 codes land raw in the upper half
+//     of their slot; warps 1-3 convert them in place, exactly, to bf16 and
+//     then release the item to the tensor core.
+//   * Warp 0 issues every tcgen05.mma; warps 4-7 (thread i = TMEM lane i =
+//     key i / dv i) apply the fp8 scales, mask, run the online softmax with a
+//     lazily moved base-2 reference, write P^T (fp8: per dv chunk with that
+//     chunk's scale, split into high and low bf16 parts) and finally normalise
+//     and store O and LSE.
 //   * Every wait is bounded; on expiry the CTA records CPMLA_ERR_TIMEOUT,
 //     drains its copies and MMAs, and exits.
 #include <cmath>
@@ -30,122 +41,162 @@ namespace cpmla {
 namespace {
 
 constexpr int kGatherWarp0 = 8;
+constexpr int kSlotBytes = 2 * kKbBytes;  // 32 KB
+constexpr int kKItems = 5;                // K of a tile: 4 k-block pairs + rope
+constexpr int kVItems = 4;                // V of a tile: 4 chunks of 128 dv
 
-// Shared-memory control block of the sparse kernel (after the operand buffers).
+template <int MODE>
+__host__ __device__ constexpr int score_accumulators() {
+  return MODE == kSparseFp8 ? 5 : 1;
+}
+
+// P^T matrices: one, or for fp8 one per dv chunk and part (high, low).
+template <int MODE, int R>
+__host__ __device__ constexpr int p_region_bytes() {
+  return (MODE == kSparseFp8 ? 8 : 1) * kTileKeys * R * 2;
+}
+
 template <int R>
-struct Ctrl {
-  uint64_t full[kKb];
-  uint64_t empty[kKb];
-  uint64_t s_full;
+struct SparseCtrl {
+  uint64_t full[8];   // item ready for the tensor core
+  uint64_t raw[8];    // fp8: item's codes landed, ready for conversion
+  uint64_t empty[8];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full;
+  uint64_t p_free;
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int n_tiles;
-  int bflag[3][2];       // elected wait results, per role, alternating slots
-  int need_rescale[2];   // per softmax warpgroup: tile index + 1 of the last rescale
-  int64_t key_row[2][kTileKeys];  // sparse: global KV row per key, -1 = masked
-  float red[2][4][32];
+  int bflag[3][2];  // elected wait results (softmax, gather, convert), alternating slots
+  int need_rescale;
+  uint64_t meta_full[2];      // key metadata of a tile written (gather -> softmax)
+  uint64_t meta_empty[2];     // key metadata of a tile read (softmax -> gather)
+  int key_row[2][kTileKeys];  // KV row per key of a tile, -1 = masked
+  float4 key_scale[2][kTileKeys];  // fp8: the key's four group scales
+  float red[4][32];
   float m_ref[R];
   float alpha[R];
   float lse[R];
   float inv_l[R];
 };
 
-// fp8 keeps eight P^T matrices in a region of their own: per 128-dv chunk,
-// P with that chunk's per-key scale folded in, split into a high and a low
-// bf16 part.
 template <int MODE, int R>
-__host__ __device__ constexpr int p_region_bytes() {
-  return MODE == kSparseFp8 ? 8 * kTileKeys * R * 2 : 0;
+__host__ __device__ constexpr int fixed_bytes() {
+  return 1024 + R * CPMLA_DQK * 2 + p_region_bytes<MODE, R>() + (int)sizeof(SparseCtrl<R>);
 }
-
+// as many 32 KB ring slots as fit (at most 8)
+template <int MODE, int R>
+__host__ __device__ constexpr int ring_slots() {
+  return (232448 - fixed_bytes<MODE, R>()) / kSlotBytes > 8
+             ? 8
+             : (232448 - fixed_bytes<MODE, R>()) / kSlotBytes;
+}
 template <int MODE, int R>
 __host__ __device__ constexpr int smem_bytes() {
-  return 1024 /*align slack*/ + R * CPMLA_DQK * 2 + kKb * kKbBytes + p_region_bytes<MODE, R>() +
-         (int)sizeof(Ctrl<R>);
+  return fixed_bytes<MODE, R>() + ring_slots<MODE, R>() * kSlotBytes;
 }
 
-// Score accumulators: one for bf16 KV; for fp8, one per 128-channel scale
-// group plus one for the rope, so the MMA only ever sees exact E4M3 values.
-template <int MODE>
-__host__ __device__ constexpr int score_accumulators() {
-  return MODE == kSparseFp8 ? 5 : 1;
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+  }
+}
+
+// Ring items in the MMA issuer's order: K(0) = items 0-4, then for each step
+// i >= 1 the K items of tile i (if i < n_tiles; the fifth is the rope) and the
+// four V items of tile i-1.  True when item m carries latent dims (fp8 codes).
+__device__ __forceinline__ bool latent_item(uint32_t m, int n_tiles) {
+  if (m < (uint32_t)kKItems) return m != (uint32_t)kKItems - 1;
+  const uint32_t r2 = (m - kKItems) % (kKItems + kVItems);
+  const uint32_t step = (m - kKItems) / (kKItems + kVItems) + 1;
+  return (int)step < n_tiles ? r2 != (uint32_t)kKItems - 1 : true;
+}
+
+// In-place E4M3 -> bf16 conversion of one latent item by the 96 threads of
+// warps 1-3: the raw codes of 128 keys x 128 dims sit unswizzled in the upper
+// half of the slot (key k at 16 KB + 128 k); the result is two 128-byte-
+// swizzled k-blocks.  Unit u = (key u/8, codes 16 (u%8) ...); the eight units
+// of a key fall in one warp in the same step, so every code of the key is read
+// (one load instruction) before its bf16 row is written over it.  The
+// conversion is exact: every E4M3 value is a bf16 value.
+__device__ __forceinline__ void convert_fp8_item(uint8_t *sl, int t) {
+#pragma unroll 1
+  for (int u = t; u < kTileKeys * 8; u += 96) {
+    const int key = u >> 3, c8 = u & 7;
+    const uint4 raw = *reinterpret_cast<const uint4 *>(sl + kKbBytes + key * 128 + c8 * 16);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f0 = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
+      const float2 f1 = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
+      o[2 * q] = pack_bf16x2(f0.x, f0.y);
+      o[2 * q + 1] = pack_bf16x2(f1.x, f1.y);
+    }
+    // dims 16 c8 .. 16 c8 + 15 of the pair: k-block c8 / 4, chunks 2 (c8 % 4), +1
+    const int kb = c8 >> 2, cc0 = 2 * (c8 & 3);
+    uint8_t *rowp = sl + kb * kKbBytes + key * 128;
+    __syncwarp();
+    *reinterpret_cast<uint4 *>(rowp + ((cc0 ^ (key & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(rowp + (((cc0 + 1) ^ (key & 7)) << 4)) =
+        make_uint4(o[4], o[5], o[6], o[7]);
+  }
 }
 
 template <int MODE, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_sparse_kernel(const __grid_constant__ AttnArgs a) {
-  // rows handled by one softmax warpgroup, and how many such warpgroups
-  constexpr int RW = R < 32 ? R : 32;
-  constexpr int NSWG = R / RW;
-  static_assert(NSWG == 1, "warps 8-11 gather, so one softmax warpgroup");
+  static_assert(R == 16 || R == 32, "one softmax warpgroup");
   constexpr int NS = score_accumulators<MODE>();
-  constexpr int kCols = R * (NS + 4);
+  constexpr int NSLOT = ring_slots<MODE, R>();
+  static_assert(NSLOT >= 3, "ring too small");
+  constexpr int kCols = 2 * NS * R + 4 * R;
   constexpr uint32_t kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
-  static_assert(kCols <= 512, "TMEM budget");
+  constexpr int kPBytes = kTileKeys * PLayout<R>::row_bytes;  // one P^T matrix
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *sQ = smem;                       // 9 k-blocks of [R x 64] bf16
-  uint8_t *sKV = smem + R * CPMLA_DQK * 2;  // 9 slots of [128 x 64] bf16
-  uint8_t *sP = MODE == kSparseFp8 ? sKV + kKb * kKbBytes : sKV + kLatKb * kKbBytes;
-  Ctrl<R> &c = *reinterpret_cast<Ctrl<R> *>(sKV + kKb * kKbBytes + p_region_bytes<MODE, R>());
+  uint8_t *sQ = smem;                             // 9 k-blocks of [R x 64] bf16
+  uint8_t *sP = sQ + R * CPMLA_DQK * 2;           // P^T matrices
+  uint8_t *sRing = sP + p_region_bytes<MODE, R>();
+  SparseCtrl<R> &c = *reinterpret_cast<SparseCtrl<R> *>(sRing + NSLOT * kSlotBytes);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int item = blockIdx.x;
-  const int row_group = item / a.n_hgroups;
-  const int hg = item - row_group * a.n_hgroups;
-  const int row0 = row_group * a.g;  // first shard row of this CTA
+  const int row = item / a.n_hgroups;  // one shard row (token) per CTA
+  const int hg = item - row * a.n_hgroups;
   const int h0 = hg * a.hc;
-  const int r_valid = a.g * a.hc;
+  const int r_valid = a.hc;
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
-    for (int b = 0; b < kKb; ++b) {
-      mbar_init(&c.full[b], 128);
-      mbar_init(&c.empty[b], 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      // bf16: the 128 gather threads' copies; fp8: the converter's release
+      mbar_init(&c.full[s], MODE == kSparseFp8 ? 1 : 128);
+      mbar_init(&c.raw[s], 128);
+      mbar_init(&c.empty[s], 1);
     }
-    mbar_init(&c.s_full, 1);
-    mbar_init(&c.p_full, 128 * NSWG);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&c.s_full[s], 1);
+      mbar_init(&c.s_free[s], 128);
+      mbar_init(&c.meta_full[s], 128);
+      mbar_init(&c.meta_empty[s], 128);
+    }
+    mbar_init(&c.p_full, 128);
+    mbar_init(&c.p_free, 1);
     mbar_init(&c.o_full, 1);
     mbar_init(&c.drain, 1);
     c.abort = 0;
-    c.need_rescale[0] = c.need_rescale[1] = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
-  if (tid < R) {
-    c.m_ref[tid] = -INFINITY;
-    c.alpha[tid] = 1.f;
-  }
-
-  // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero padding rows)
-  for (int idx = tid; idx < R * (CPMLA_DQK / 8); idx += kThreads) {
-    const int r = idx / (CPMLA_DQK / 8);
-    const int ch = idx - r * (CPMLA_DQK / 8);  // 16-byte chunk along the 576 dims
-    const int l = r / a.hc, hh = r - l * a.hc;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < r_valid && row0 + l < a.n_rows) {
-      const int64_t gtok = a.rows[row0 + l];
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + gtok * a.q_stride +
-                                                         (int64_t)(h0 + hh) * CPMLA_DQK) +
-                         ch;
-      v = __ldg(src);
-    }
-    const int kb = ch >> 3, cc = ch & 7;
-    *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
-  }
-
-  // number of 128-key tiles of the item
-  if (tid == 0) {
+    c.need_rescale = 0;
     // last non-empty slot of the token's top-k list
     int last = -1;
-    if (row0 < a.n_rows) {
-      const int32_t *lst = a.topk + (int64_t)a.rows[row0] * a.k;
+    if (row < a.n_rows) {
+      const int32_t *lst = a.topk + (int64_t)a.rows[row] * a.k;
       for (int e = a.k - 1; e >= 0; --e)
         if (lst[e] >= 0) {
           last = e;
@@ -153,6 +204,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     c.n_tiles = (last + kTileKeys) / kTileKeys;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
+  if (tid < R) {
+    c.m_ref[tid] = -INFINITY;
+    c.alpha[tid] = 1.f;
+  }
+  // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero padding rows)
+  for (int idx = tid; idx < R * (CPMLA_DQK / 8); idx += kThreads) {
+    const int r = idx / (CPMLA_DQK / 8);
+    const int ch = idx - r * (CPMLA_DQK / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < r_valid && row < a.n_rows) {
+      const int64_t gtok = a.rows[row];
+      v = __ldg(reinterpret_cast<const uint4 *>(a.q + gtok * a.q_stride +
+                                                (int64_t)(h0 + r) * CPMLA_DQK) +
+                ch);
+    }
+    const int kb = ch >> 3, cc = ch & 7;
+    *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
   }
   fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
   tc_fence_before();
@@ -160,8 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
   const int n_tiles = c.n_tiles;
-  const uint32_t tS = tmem;           // S^T: NS accumulators of R columns
-  const uint32_t tO = tmem + NS * R;  // O^T: 4 chunks of R columns
+  const uint32_t tO = tmem + 2 * NS * R;  // O^T chunk ch at tO + ch*R; S^T buffer b at tmem + b*NS*R
   volatile int *abort = &c.abort;
 
   if (warp == 0) {
@@ -169,111 +239,153 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, R, 0, 0);
       constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
-      const uint32_t q_base = smem_u32(sQ);
-      const uint32_t kv_base = smem_u32(sKV);
-      const uint32_t p_base = smem_u32(sP);
-      constexpr int p_bytes = kTileKeys * PLayout<R>::row_bytes;  // one P^T matrix
+      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
+      const uint32_t ring = smem_u32(sRing);
+      uint32_t n = 0;  // ring items consumed
       bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const uint32_t par = j & 1;
-        // S^T = K_j . Q^T over the 9 k-blocks (latent first, rope last)
-        for (int b = 0; b < kKb; ++b) {
-          if (!mbar_wait(&c.full[b], par, abort, a.status)) {
+      for (int i = 0; i <= n_tiles && ok; ++i) {
+        if (i < n_tiles) {
+          const int sb = i & 1;
+          if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // fp8: k-blocks 2g, 2g+1 feed accumulator g, the rope feeds 4
-          const uint32_t d_acc = NS == 1 ? tS : tS + (b < kLatKb ? (b >> 1) : 4) * R;
-          const bool first_kb = NS == 1 ? b == 0 : (b == kLatKb || (b & 1) == 0);
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint64_t da = smem_desc(kv_base + b * kKbBytes + s * 32, 16, 1024, kSwz128);
-            const uint64_t db = smem_desc(q_base + b * (R * 128) + s * 32, 16, 1024, kSwz128);
-            mma_bf16_ss(d_acc, da, db, id_qk, (first_kb && s == 0) ? 0u : 1u);
-          }
-        }
-        if (!ok) break;
-        mma_commit(&c.s_full);
-        // O^T += V_j^T . P_j^T, four 128-dv chunks
-        if (!mbar_wait(&c.p_full, par, abort, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-          for (int s = 0; s < kTileKeys / 16; ++s) {
-            const uint64_t da = smem_desc(kv_base + (2 * ch) * kKbBytes + s * 2048,
-                                          kKbBytes /*next 64 dv*/, 1024, kSwz128);
-#pragma unroll
-            for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
-              const uint32_t pm = p_base + (MODE == kSparseFp8 ? (2 * ch + part) * p_bytes : 0);
-              const uint64_t db = smem_desc(pm + s * 16 * PLayout<R>::row_bytes, 8192,
-                                            8 * PLayout<R>::row_bytes, PLayout<R>::swz);
-              mma_bf16_ss(tO + ch * R, da, db, id_pv, (j > 0 || s > 0 || part > 0) ? 1u : 0u);
+          const uint32_t dS = tmem + sb * NS * R;
+          for (int pr = 0; pr < kKItems; ++pr, ++n) {
+            const uint32_t slot = n % NSLOT;
+            if (!mbar_wait(&c.full[slot], (n / NSLOT) & 1, abort, a.status)) {
+              ok = false;
+              break;
             }
+            // the slot was written through the generic proxy (cp.async or
+            // the converter's stores); order it before the tensor core reads
+            fence_proxy_async_smem();
+            tc_fence_after();
+            // fp8: pair pr (one 128-channel scale group) feeds accumulator pr,
+            // the rope feeds accumulator 4
+            const uint32_t d_acc = NS == 1 ? dS : dS + pr * R;
+            const int nkb = pr < 4 ? 2 : 1;
+            for (int h = 0; h < nkb; ++h) {
+              const int b = 2 * pr + h;  // k-block (8 = rope)
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const uint64_t da =
+                    smem_desc(ring + slot * kSlotBytes + h * kKbBytes + s * 32, 16, 1024, kSwz128);
+                const uint64_t db = smem_desc(q_base + b * (R * 128) + s * 32, 16, 1024, kSwz128);
+                const bool first = NS == 1 ? (b == 0 && s == 0) : (h == 0 && s == 0);
+                mma_bf16_ss(d_acc, da, db, id_qk, first ? 0u : 1u);
+              }
+            }
+            mma_commit(&c.empty[slot]);
           }
-          mma_commit(&c.empty[2 * ch]);
-          mma_commit(&c.empty[2 * ch + 1]);
+          if (!ok) break;
+          mma_commit(&c.s_full[sb]);
         }
-        mma_commit(&c.empty[kLatKb]);
+        if (i >= 1) {
+          const int j = i - 1;
+          if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int ch = 0; ch < kVItems; ++ch, ++n) {
+            const uint32_t slot = n % NSLOT;
+            if (!mbar_wait(&c.full[slot], (n / NSLOT) & 1, abort, a.status)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();
+            tc_fence_after();
+#pragma unroll
+            for (int s = 0; s < kTileKeys / 16; ++s) {
+              const uint64_t da = smem_desc(ring + slot * kSlotBytes + s * 2048, kKbBytes, 1024,
+                                            kSwz128);
+#pragma unroll
+              for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
+                const uint32_t pm = p_base + (MODE == kSparseFp8 ? (2 * ch + part) * kPBytes : 0);
+                const uint64_t db = smem_desc(pm + s * 16 * PLayout<R>::row_bytes, 8192,
+                                              8 * PLayout<R>::row_bytes, PLayout<R>::swz);
+                mma_bf16_ss(tO + ch * R, da, db, id_pv,
+                            (j > 0 || s > 0 || part > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(&c.empty[slot]);
+          }
+          if (!ok) break;
+          mma_commit(&c.p_free);
+        }
       }
       mma_commit(&c.o_full);
       if (!ok) {
-        // let this thread's issued MMAs finish before TMEM and SMEM go away
         mma_commit(&c.drain);
-        unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(&c.drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
-        }
+        drain_wait(&c.drain, 0);
       }
     }
     __syncwarp();
-  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4 * NSWG) {
+  } else if (warp >= 1 && warp <= 3) {
+    // ---------------------------------------------------- fp8 converter
+    if (MODE == kSparseFp8) {
+      const int t = tid - 32;
+      int seq = 0;
+      uint32_t total = 0;  // items of the whole item sequence
+      if (n_tiles > 0) total = (uint32_t)(n_tiles * (kKItems + kVItems));
+      for (uint32_t m = 0; m < total; ++m) {
+        const uint32_t slot = m % NSLOT;
+        // elected wait on the raw codes, shared by the 96 threads
+        int *f = c.bflag[2] + (seq & 1);
+        ++seq;
+        if (t == 0) *f = mbar_wait(&c.raw[slot], (m / NSLOT) & 1, abort, a.status) ? 1 : 0;
+        named_bar_sync(4, 96);
+        if (!*reinterpret_cast<volatile int *>(f)) break;
+        fence_proxy_async_smem();
+        if (latent_item(m, n_tiles)) convert_fp8_item(sRing + slot * kSlotBytes, t);
+        fence_proxy_async_smem();
+        named_bar_sync(4, 96);
+        if (t == 0) mbar_arrive(&c.full[slot]);
+      }
+    }
+  } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
     // ---------------------------------------------------- softmax + epilogue
-    // warpgroup wg owns S^T / O^T columns [wg*RW, wg*RW + RW); thread t owns
-    // TMEM lane t (key t of a tile, dv t of an O^T chunk)
-    const int wg = (warp - kSoftmaxWarp0) >> 2;
-    const int t = tid - kSoftmaxWarp0 * 32 - wg * 128;
-    const int q4 = (warp - kSoftmaxWarp0) & 3;  // TMEM lane quarter
+    const int t = tid - kSoftmaxWarp0 * 32;
+    const int q4 = warp - kSoftmaxWarp0;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int cbase = wg * RW;  // first row (column) of this warpgroup
-    const int bar_id = 1 + wg;
     int seq = 0;
-    float l_part[RW];
+    float l_part[R];
 #pragma unroll
-    for (int r = 0; r < RW; ++r) l_part[r] = 0.f;
+    for (int r = 0; r < R; ++r) l_part[r] = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      if (!group_wait(&c.s_full, j & 1, t, bar_id, c.bflag[wg], seq, abort, a.status)) {
+      const int sb = j & 1;
+      if (!group_wait(&c.s_full[sb], (j >> 1) & 1, t, 1, c.bflag[0], seq, abort, a.status) ||
+          !group_wait(&c.meta_full[sb], (j >> 1) & 1, t, 1, c.bflag[0], seq, abort, a.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[RW];
+      const uint32_t tS = tmem + sb * NS * R + lane_off;
+      const int src = c.key_row[sb][t];
+      float s[R];
       float ksc[4] = {1.f, 1.f, 1.f, 1.f};  // fp8: this key's group scales
       if (NS == 1) {
 #pragma unroll
-        for (int cc = 0; cc < RW / 16; ++cc)
-          tmem_ld16(tS + lane_off + cbase + cc * 16, s + cc * 16);
+        for (int cc = 0; cc < R / 16; ++cc) tmem_ld16(tS + cc * 16, s + cc * 16);
         tmem_ld_wait();
       } else {
-        // s = rope part + sum_g scale_g * (q . e4m3 codes of group g)
-        const int64_t src = sparse_key_src(a, row0, j * kTileKeys + t);
-        if (src >= 0) {
-          const float4 sc4 = __ldg(reinterpret_cast<const float4 *>(a.kv_scale) + src);
+        // s = rope part + sum_g scale_g * (q . E4M3 codes of group g)
+        {
+          const float4 sc4 = c.key_scale[sb][t];
           ksc[0] = sc4.x;
           ksc[1] = sc4.y;
           ksc[2] = sc4.z;
           ksc[3] = sc4.w;
         }
 #pragma unroll
-        for (int cc = 0; cc < RW / 16; ++cc) {
-          tmem_ld16(tS + lane_off + 4 * R + cbase + cc * 16, s + cc * 16);
+        for (int cc = 0; cc < R / 16; ++cc) {
+          tmem_ld16(tS + 4 * R + cc * 16, s + cc * 16);
           float part[4][16];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) tmem_ld16(tS + lane_off + g * R + cbase + cc * 16, part[g]);
+          for (int g = 0; g < 4; ++g) tmem_ld16(tS + g * R + cc * 16, part[g]);
           tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 16; ++x)
@@ -281,78 +393,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                               ksc[3] * part[3][x];
         }
       }
-      // mask, scale to log2 units
+      tc_fence_before();
+      mbar_arrive(&c.s_free[sb]);  // the next-but-one score GEMM may overwrite it
       {
-        const bool valid = sparse_key_src(a, row0, j * kTileKeys + t) >= 0;
+        const bool valid = src >= 0;
 #pragma unroll
-        for (int r = 0; r < RW; ++r)
-          s[r] = (valid && cbase + r < r_valid) ? s[r] * a.scale_log2 : -INFINITY;
+        for (int r = 0; r < R; ++r)
+          s[r] = (valid && r < r_valid) ? s[r] * a.scale_log2 : -INFINITY;
       }
-      // row maxima over the tile's 128 keys
       {
-        float v[RW];
+        float v[R];
 #pragma unroll
-        for (int r = 0; r < RW; ++r) v[r] = s[r];
-        warp_transpose_reduce<RW, true>(v, lane);
-        if (RW == 32 || (lane & 1) == 0) c.red[wg][q4][RW == 32 ? lane : (lane >> 1)] = v[0];
+        for (int r = 0; r < R; ++r) v[r] = s[r];
+        warp_transpose_reduce<R, true>(v, lane);
+        if (R == 32 || (lane & 1) == 0) c.red[q4][R == 32 ? lane : (lane >> 1)] = v[0];
       }
-      named_bar_sync(bar_id, 128);
-      if (t < RW) {
-        const int r = cbase + t;
-        const float tile_max = fmaxf(fmaxf(c.red[wg][0][t], c.red[wg][1][t]),
-                                     fmaxf(c.red[wg][2][t], c.red[wg][3][t]));
-        const float m_old = c.m_ref[r];
+      named_bar_sync(1, 128);
+      if (t < R) {
+        const float tile_max =
+            fmaxf(fmaxf(c.red[0][t], c.red[1][t]), fmaxf(c.red[2][t], c.red[3][t]));
+        const float m_old = c.m_ref[t];
         float m_new = m_old;
         if (tile_max > m_old + 8.f) m_new = tile_max;  // lazy move of the reference
-        c.alpha[r] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
-        c.m_ref[r] = m_new;
-        if (j > 0 && m_new != m_old) c.need_rescale[wg] = j + 1;
+        c.alpha[t] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
+        c.m_ref[t] = m_new;
+        if (j > 0 && m_new != m_old) c.need_rescale = j + 1;
       }
-      named_bar_sync(bar_id, 128);
-      const bool rescale = c.need_rescale[wg] == j + 1;
-      // p = 2^(s - m_ref); per-lane partial row sums
+      named_bar_sync(1, 128);
+      const bool rescale = c.need_rescale == j + 1;
       // (s is overwritten with p)
-      uint32_t pk[RW / 2];
+      uint32_t pk[R / 2];
 #pragma unroll
-      for (int r = 0; r < RW; r += 2) {
-        const float m0 = c.m_ref[cbase + r], m1 = c.m_ref[cbase + r + 1];
+      for (int r = 0; r < R; r += 2) {
+        const float m0 = c.m_ref[r], m1 = c.m_ref[r + 1];
         const float p0 = fast_exp2(s[r] - (m0 == -INFINITY ? 0.f : m0));
         const float p1 = fast_exp2(s[r + 1] - (m1 == -INFINITY ? 0.f : m1));
         if (NS == 1) pk[r / 2] = pack_bf16x2(p0, p1);
-        l_part[r] = l_part[r] * c.alpha[cbase + r] + p0;
-        l_part[r + 1] = l_part[r + 1] * c.alpha[cbase + r + 1] + p1;
+        l_part[r] = l_part[r] * c.alpha[r] + p0;
+        l_part[r + 1] = l_part[r + 1] * c.alpha[r + 1] + p1;
         s[r] = p0;
         s[r + 1] = p1;
       }
+      // PV(j-1) must be done before P^T is overwritten or O^T rescaled
+      if (j >= 1 && !group_wait(&c.p_free, (j - 1) & 1, t, 1, c.bflag[0], seq, abort, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       if (rescale) {
-        // O^T columns *= alpha; PV(j-1) is complete (QK(j) was issued after it)
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
 #pragma unroll
-          for (int cc = 0; cc < RW / 16; ++cc) {
+          for (int cc = 0; cc < R / 16; ++cc) {
             float o[16];
-            const uint32_t col = tO + lane_off + ch * R + cbase + cc * 16;
+            const uint32_t col = tO + lane_off + ch * R + cc * 16;
             tmem_ld16(col, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 16; ++x) o[x] *= c.alpha[cbase + cc * 16 + x];
+            for (int x = 0; x < 16; ++x) o[x] *= c.alpha[cc * 16 + x];
             tmem_st16(col, o);
           }
         }
         tmem_st_wait();
       }
-      // this warpgroup's part of P^T row t, into the rope slot (the score
-      // GEMM of tile j has consumed it)
 #pragma unroll
       for (int m = 0; m < (NS == 1 ? 1 : 8); ++m) {
-        uint8_t *prow = sP + m * (kTileKeys * PLayout<R>::row_bytes) + t * PLayout<R>::row_bytes;
+        uint8_t *prow = sP + m * kPBytes + t * PLayout<R>::row_bytes;
         if (NS != 1) {
-          // P^T of dv chunk m/2: p times this key's scale of channel group m/2,
-          // as a high bf16 part (m even) and the bf16 rounding of the rest (m
-          // odd); the PV GEMM adds both, so P reaches the tensor core with ~16
-          // significant bits
+          // P^T of dv chunk m/2: p times this key's scale of channel group
+          // m/2, as a high bf16 part (m even) and the bf16 rounding of the
+          // rest (m odd); the PV GEMM adds both, so P reaches the tensor core
+          // with ~16 significant bits
 #pragma unroll
-          for (int r = 0; r < RW; r += 2) {
+          for (int r = 0; r < R; r += 2) {
             const float x0 = s[r] * ksc[m >> 1], x1 = s[r + 1] * ksc[m >> 1];
             const uint32_t hi = pack_bf16x2(x0, x1);
             pk[r / 2] = (m & 1) ? pack_bf16x2(x0 - __uint_as_float(hi << 16),
@@ -361,9 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int ch = 0; ch < RW / 8; ++ch) {
-          const int logical = wg * (RW / 8) + ch;
-          const int phys = logical ^ PLayout<R>::chunk_xor(t);
+        for (int ch = 0; ch < R / 8; ++ch) {
+          const int phys = ch ^ PLayout<R>::chunk_xor(t);
           *reinterpret_cast<uint4 *>(prow + phys * 16) =
               make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
         }
@@ -371,35 +483,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&c.p_full);
+      mbar_arrive(&c.meta_empty[sb]);  // done with this tile's key metadata
     }
     // ------------------------------------------------ epilogue
-    if (ok) ok = group_wait(&c.o_full, 0, t, bar_id, c.bflag[wg], seq, abort, a.status);
+    if (ok) ok = group_wait(&c.o_full, 0, t, 1, c.bflag[0], seq, abort, a.status);
     if (ok) {
       tc_fence_after();
-      warp_transpose_reduce<RW, false>(l_part, lane);
-      if (RW == 32 || (lane & 1) == 0) c.red[wg][q4][RW == 32 ? lane : (lane >> 1)] = l_part[0];
-      named_bar_sync(bar_id, 128);
-      if (t < RW) {
-        const int r = cbase + t;
-        const float l = c.red[wg][0][t] + c.red[wg][1][t] + c.red[wg][2][t] + c.red[wg][3][t];
-        const float m = c.m_ref[r];
+      warp_transpose_reduce<R, false>(l_part, lane);
+      if (R == 32 || (lane & 1) == 0) c.red[q4][R == 32 ? lane : (lane >> 1)] = l_part[0];
+      named_bar_sync(1, 128);
+      if (t < R) {
+        const float l = c.red[0][t] + c.red[1][t] + c.red[2][t] + c.red[3][t];
+        const float m = c.m_ref[t];
         const bool empty = !(l > 0.f) || m == -INFINITY;
-        c.lse[r] = empty ? -INFINITY : (m + __log2f(l)) * 0.69314718055994530942f;
-        c.inv_l[r] = empty ? 0.f : 1.f / l;
-        if (r < r_valid) {
-          const int lrow = r / a.hc, hh = r - lrow * a.hc;
-          const int i = row0 + lrow;
-          if (i < a.n_rows) a.lse_part[(int64_t)i * a.H + h0 + hh] = c.lse[r];
-        }
+        c.lse[t] = empty ? -INFINITY : (m + __log2f(l)) * 0.69314718055994530942f;
+        c.inv_l[t] = empty ? 0.f : 1.f / l;
+        if (t < r_valid && row < a.n_rows) a.lse_part[(int64_t)row * a.H + h0 + t] = c.lse[t];
       }
-      named_bar_sync(bar_id, 128);
+      named_bar_sync(1, 128);
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
 #pragma unroll
-        for (int cc = 0; cc < RW / 16; ++cc) {
+        for (int cc = 0; cc < R / 16; ++cc) {
           float o[16];
           if (n_tiles > 0) {
-            tmem_ld16(tO + lane_off + ch * R + cbase + cc * 16, o);
+            tmem_ld16(tO + lane_off + ch * R + cc * 16, o);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -407,92 +515,110 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
-            const int r = cbase + cc * 16 + x;
-            if (r < r_valid) {
-              const int lrow = r / a.hc, hh = r - lrow * a.hc;
-              const int i = row0 + lrow;
-              if (i < a.n_rows)
-                a.o_part[((int64_t)i * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
-                    o[x] * c.inv_l[r];
-            }
+            const int r = cc * 16 + x;
+            if (r < r_valid && row < a.n_rows)
+              a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
+                  o[x] * c.inv_l[r];
           }
         }
       }
     }
   } else if (warp >= kGatherWarp0) {
-    // ---------------------------------------------------- sparse gather producer
+    // ---------------------------------------------------- gather producer
+    // items in the MMA issuer's order: K(0), then per i >= 1 K(i) (if any)
+    // followed by V(i-1); item n goes to slot n % NSLOT
     const int t = tid - kGatherWarp0 * 32;
-    const int row = row0;
-    const int64_t gtok = a.rows[row];
-    const int32_t *lst = a.topk + gtok * a.k;
     const int tpos = a.pos[row];
     const int64_t base = a.kv_start[a.req[row]];
+    const int32_t *lst = a.topk + (int64_t)a.rows[row] * a.k;
+    const int lo = a.kv_lo ? a.kv_lo[row] : 0;
+    const int hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
     int seq = 0;
+    uint32_t n = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      // validity and source row of key t of this tile.  Slot j&1 was last read
-      // by the softmax of tile j-2, which finished before tile j-1's slots
-      // were released, i.e. before this warpgroup got here.
-      {
-        const int e = j * kTileKeys + t;
-        const int p = e < a.k ? lst[e] : -1;
-        if (p >= 0 && (p > tpos || base + p >= a.s_kv)) record_status(a.status, CPMLA_ERR_INDEX);
-        c.key_row[j & 1][t] = sparse_key_src(a, row, e);
-      }
-      named_bar_sync(3, 128);
-      for (int b = 0; b < kKb; ++b) {
-        if (j > 0 &&
-            !group_wait(&c.empty[b], (j - 1) & 1, t, 3, c.bflag[2], seq, abort, a.status)) {
-          ok = false;
-          break;
-        }
-        uint8_t *slot = sKV + b * kKbBytes;
-        // 128 keys x 8 chunks of 16 B; a warp covers 4 keys x 128 B per step
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int key = it * 16 + (t >> 3);
-          const int cc = t & 7;
-          const int64_t src = c.key_row[j & 1][key];
-          uint8_t *dst = slot + key * 128 + ((cc ^ (key & 7)) << 4);
-          if (MODE == kSparseBf16 || b == kLatKb) {
-            const __nv_bfloat16 *gp;
-            if (MODE == kSparseBf16)
-              gp = a.kv + (src >= 0 ? src : 0) * CPMLA_DQK + b * kKbDims + cc * 8;
-            else
-              gp = a.kv_rope + (src >= 0 ? src : 0) * CPMLA_DROPE + cc * 8;
-            cp_async_16(dst, gp, src >= 0 ? 16u : 0u);
-          } else {
-            // fp8 latent: 8 codes -> 8 bf16, exactly (every E4M3 value is a
-            // bf16 value); the group scales are applied to the scores and to
-            // P^T instead
-            uint4 outv = make_uint4(0, 0, 0, 0);
-            if (src >= 0) {
-              const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(
-                  a.kv8 + src * CPMLA_DV + b * kKbDims + cc * 8));
-              const float2 f0 = e4m3x2_to_float2((uint16_t)(raw.x & 0xFFFFu));
-              const float2 f1 = e4m3x2_to_float2((uint16_t)(raw.x >> 16));
-              const float2 f2 = e4m3x2_to_float2((uint16_t)(raw.y & 0xFFFFu));
-              const float2 f3 = e4m3x2_to_float2((uint16_t)(raw.y >> 16));
-              outv = make_uint4(pack_bf16x2(f0.x, f0.y), pack_bf16x2(f1.x, f1.y),
-                                pack_bf16x2(f2.x, f2.y), pack_bf16x2(f3.x, f3.y));
-            }
-            *reinterpret_cast<uint4 *>(dst) = outv;
+    for (int i = 0; i <= n_tiles && ok; ++i) {
+      for (int part = 0; part < 2 && ok; ++part) {
+        const bool is_k = part == 0;
+        if (is_k ? i >= n_tiles : i == 0) continue;
+        const int tile = is_k ? i : i - 1;
+        if (is_k) {
+          // the KV row (and fp8 scales) of key t of this tile
+          const int e = tile * kTileKeys + t;
+          const int p = e < a.k ? lst[e] : -1;
+          int src = -1;
+          if (p >= 0) {
+            if (p > tpos || base + p >= a.s_kv)
+              record_status(a.status, CPMLA_ERR_INDEX);
+            else if (p >= lo && p <= hi)
+              src = (int)(base + p);
           }
+          float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (MODE == kSparseFp8 && src >= 0)
+            sc = __ldg(reinterpret_cast<const float4 *>(a.kv_scale) + src);
+          // the softmax of tile-2 must be done with this metadata slot
+          if (tile >= 2 && !group_wait(&c.meta_empty[tile & 1], ((tile >> 1) - 1) & 1, t, 3,
+                                       c.bflag[1], seq, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          c.key_row[tile & 1][t] = src;
+          if (MODE == kSparseFp8) c.key_scale[tile & 1][t] = sc;
+          mbar_arrive(&c.meta_full[tile & 1]);
+          named_bar_sync(3, 128);
         }
-        cp_async_commit();
-        // k-block b-1 has landed: publish it to the tensor core
-        if (b > 0) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&c.full[b - 1]);
-        }
+        const int *krow = c.key_row[tile & 1];
+        const int items = is_k ? kKItems : kVItems;
+        for (int it = 0; it < items; ++it, ++n) {
+          const uint32_t slot = n % NSLOT;
+          if (n >= (uint32_t)NSLOT &&
+              !group_wait(&c.empty[slot], ((n / NSLOT) - 1) & 1, t, 3, c.bflag[1], seq, abort,
+                          a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *dst = sRing + slot * kSlotBytes;
+          const bool rope = is_k && it == kKItems - 1;
+          if (rope) {
+            // 128 keys x 8 chunks of 16 B, a warp covering 4 keys per step
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+              const int key = st * 16 + (t >> 3), cc = t & 7;
+              const int src = krow[key];
+              const __nv_bfloat16 *gp =
+                  MODE == kSparseBf16
+                      ? a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + CPMLA_DV + cc * 8
+                      : a.kv_rope + (int64_t)(src >= 0 ? src : 0) * CPMLA_DROPE + cc * 8;
+              cp_async_16(dst + key * 128 + ((cc ^ (key & 7)) << 4), gp, src >= 0 ? 16u : 0u);
+            }
+          } else if (MODE == kSparseBf16) {
+            // dims [128 it, 128 it + 128) of 128 keys: 16 chunks per key, a
+            // warp covering 2 keys x 256 B per step; two swizzled k-blocks
+#pragma unroll
+            for (int st = 0; st < 16; ++st) {
+              const int key = st * 8 + (t >> 4), c16 = t & 15;
+              const int kb = c16 >> 3, cc = c16 & 7;
+              const int src = krow[key];
+              cp_async_16(dst + kb * kKbBytes + key * 128 + ((cc ^ (key & 7)) << 4),
+                          a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + it * 128 + c16 * 8,
+                          src >= 0 ? 16u : 0u);
+            }
+          } else {
+            // raw E4M3 codes of dims [128 it, 128 it + 128): 128 B per key,
+            // unswizzled, in the upper half of the slot
+#pragma unroll
+            for (int st = 0; st < 8; ++st) {
+              const int key = st * 16 + (t >> 3), c8 = t & 7;
+              const int src = krow[key];
+              cp_async_16(dst + kKbBytes + key * 128 + c8 * 16,
+                          a.kv8 + (int64_t)(src >= 0 ? src : 0) * CPMLA_DV + it * 128 + c8 * 16,
+                          src >= 0 ? 16u : 0u);
+            }
+          }
+          // the item's barrier hears from this thread once its copies land
+          cp_async_arrive_noinc(MODE == kSparseFp8 ? &c.raw[slot] : &c.full[slot]);        }
       }
-      if (!ok) break;
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(&c.full[kKb - 1]);
     }
-    cp_async_wait<0>();
+    cp_async_wait<0>();  // own copies in flight, before the CTA may exit
   }
 
   // ------------------------------------------------------------ teardown
@@ -503,7 +629,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
 }
-
 
 template <int MODE, int R>
 int launch_t(const AttnArgs &args, int n_items, cudaStream_t stream) {

@@ -115,6 +115,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// TMA gather of four rows (r0..r3) of a 2D tensor, box = one row of the
+// tensor map's box width starting at column x; the rows land contiguously.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *tm, int x, int r0, int r1,
+                                            int r2, int r3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -123,6 +134,12 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                "r"(src_bytes)
+               : "memory");
+}
+// Arrive on an mbarrier once every cp.async issued so far by this thread has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
