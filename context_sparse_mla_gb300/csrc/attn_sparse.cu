@@ -8,24 +8,28 @@
 // fp8 KV cache.
 //
 // One CTA = one token x up to 32 heads (16 for fp8): its keys are its own, so
-// a KV tile serves only that token's heads.  The pipeline is the dense
-// kernel's, fed by a gather instead of TMA:
+// a KV tile serves only that token's heads.  The load/store-unit gather is
+// the scarce resource (its copies queue in the memory pipeline), so every key
+// row is gathered once: the latent k-blocks stay resident from the score GEMM
+// to the PV GEMM.
 //   * Score GEMM key-major: S^T = K . Q^T, M = 128 keys, N = R rows, K = 576,
-//     into one of two TMEM buffers, so the score GEMM of tile j+1 overlaps the
-//     softmax of tile j.  fp8 keeps one fp32 accumulator per 128-channel scale
-//     group and one for the rope, so the MMA only sees exact E4M3 values.  PV
-//     GEMM: O^T += V^T . P^T, M = 128 dv x 4 chunks, N = R, K = 128 keys.
-//   * One ring of 32 KB slots carries what the tensor core reads, in the order
-//     it reads it: K of a tile as five items (128-dim pairs of k-blocks
-//     [128 keys x 64 dims], the rope alone) and V of the previous tile as four
-//     128-dv chunks, gathered again (the same bytes as K pairs 0-3).
-//   * Warps 8-11 gather: once per tile they resolve the 128 keys' KV rows
-//     (and fp8 scales) into shared memory for everyone, then issue each item
-//     with cp.async by all 128 threads, whose completion arrives on the item's
-//     barrier by itself (cp.async.mbarrier.arrive.noinc), so the gather runs
-//     as far ahead as the ring allows.  fp8 codes land raw in the upper half
-//     of their slot; warps 1-3 convert them in place, exactly, to bf16 and
-//     then release the item to the tensor core.
+//     into one of two TMEM buffers.  fp8 keeps one fp32 accumulator per
+//     128-channel scale group and one for the rope, so the MMA only sees exact
+//     E4M3 values.  PV GEMM: O^T += V^T . P^T, M = 128 dv x 4 chunks, N = R,
+//     K = 128 keys, reading V from the same k-blocks.
+//   * Shared memory holds a ring of 32 KB pair slots (two k-blocks
+//     [128 keys x 64 dims] each) and one rope slot.  Pair p of tile j sits at
+//     ring position 4j + p, so with five or more slots the first pairs of tile
+//     j+1 are gathered while tile j still holds its four.  The score GEMM of
+//     tile j+1 is issued in two parts around the PV GEMM of tile j: the rope
+//     and the pairs already in flight before it, the rest after it frees
+//     their slots.
+//   * Warps 8-11 gather: per tile they resolve the 128 keys' KV rows (and
+//     fp8 scales) into shared memory, then issue the rope and the four pairs
+//     with cp.async, each thread's completion arriving on the slot's barrier
+//     by itself (cp.async.mbarrier.arrive.noinc).  fp8 codes land raw in the
+//     upper half of their pair slot; warps 1-3 convert them in place, exactly,
+//     to bf16 and release the slot to the tensor core.
 //   * Warp 0 issues every tcgen05.mma; warps 4-7 (thread i = TMEM lane i =
 //     key i / dv i) apply the fp8 scales, mask, run the online softmax with a
 //     lazily moved base-2 reference, write P^T (fp8: per dv chunk with that
@@ -41,9 +45,8 @@ namespace cpmla {
 namespace {
 
 constexpr int kGatherWarp0 = 8;
-constexpr int kSlotBytes = 2 * kKbBytes;  // 32 KB
-constexpr int kKItems = 5;                // K of a tile: 4 k-block pairs + rope
-constexpr int kVItems = 4;                // V of a tile: 4 chunks of 128 dv
+constexpr int kSlotBytes = 2 * kKbBytes;  // 32 KB pair slot
+constexpr int kPairs = 4;                 // latent k-block pairs per tile
 
 template <int MODE>
 __host__ __device__ constexpr int score_accumulators() {
@@ -56,26 +59,28 @@ __host__ __device__ constexpr int p_region_bytes() {
   return (MODE == kSparseFp8 ? 8 : 1) * kTileKeys * R * 2;
 }
 
-template <int R>
+template <int MODE, int R>
 struct SparseCtrl {
-  uint64_t full[8];   // item ready for the tensor core
-  uint64_t raw[8];    // fp8: item's codes landed, ready for conversion
-  uint64_t empty[8];
+  uint64_t full[8];    // pair slot ready for the tensor core
+  uint64_t raw[8];     // fp8: pair slot's codes landed, ready for conversion
+  uint64_t empty[8];   // pair slot released by the PV GEMM
+  uint64_t rope_full;
+  uint64_t rope_empty;
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t p_free;
   uint64_t o_full;
   uint64_t drain;
+  uint64_t meta_full[2];   // key metadata of a tile written (gather -> softmax)
+  uint64_t meta_empty[2];  // key metadata of a tile read (softmax -> gather)
   uint32_t tmem_base;
   int abort;
   int n_tiles;
   int bflag[3][2];  // elected wait results (softmax, gather, convert), alternating slots
   int need_rescale;
-  uint64_t meta_full[2];      // key metadata of a tile written (gather -> softmax)
-  uint64_t meta_empty[2];     // key metadata of a tile read (softmax -> gather)
   int key_row[2][kTileKeys];  // KV row per key of a tile, -1 = masked
-  float4 key_scale[2][kTileKeys];  // fp8: the key's four group scales
+  float4 key_scale[MODE == kSparseFp8 ? 2 : 1][MODE == kSparseFp8 ? kTileKeys : 1];
   float red[4][32];
   float m_ref[R];
   float alpha[R];
@@ -85,34 +90,25 @@ struct SparseCtrl {
 
 template <int MODE, int R>
 __host__ __device__ constexpr int fixed_bytes() {
-  return 1024 + R * CPMLA_DQK * 2 + p_region_bytes<MODE, R>() + (int)sizeof(SparseCtrl<R>);
+  return 1024 + R * CPMLA_DQK * 2 + p_region_bytes<MODE, R>() + kKbBytes /*rope slot*/ +
+         (int)sizeof(SparseCtrl<MODE, R>);
 }
-// as many 32 KB ring slots as fit (at most 8)
+// as many pair slots as fit (4 to 8)
 template <int MODE, int R>
-__host__ __device__ constexpr int ring_slots() {
+__host__ __device__ constexpr int pair_slots() {
   return (232448 - fixed_bytes<MODE, R>()) / kSlotBytes > 8
              ? 8
              : (232448 - fixed_bytes<MODE, R>()) / kSlotBytes;
 }
 template <int MODE, int R>
 __host__ __device__ constexpr int smem_bytes() {
-  return fixed_bytes<MODE, R>() + ring_slots<MODE, R>() * kSlotBytes;
+  return fixed_bytes<MODE, R>() + pair_slots<MODE, R>() * kSlotBytes;
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   unsigned long long t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
   }
-}
-
-// Ring items in the MMA issuer's order: K(0) = items 0-4, then for each step
-// i >= 1 the K items of tile i (if i < n_tiles; the fifth is the rope) and the
-// four V items of tile i-1.  True when item m carries latent dims (fp8 codes).
-__device__ __forceinline__ bool latent_item(uint32_t m, int n_tiles) {
-  if (m < (uint32_t)kKItems) return m != (uint32_t)kKItems - 1;
-  const uint32_t r2 = (m - kKItems) % (kKItems + kVItems);
-  const uint32_t step = (m - kKItems) / (kKItems + kVItems) + 1;
-  return (int)step < n_tiles ? r2 != (uint32_t)kKItems - 1 : true;
 }
 
 // In-place E4M3 -> bf16 conversion of one latent item by the 96 threads of
@@ -151,8 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mla_sparse_kernel(const __grid_constant__ AttnArgs a) {
   static_assert(R == 16 || R == 32, "one softmax warpgroup");
   constexpr int NS = score_accumulators<MODE>();
-  constexpr int NSLOT = ring_slots<MODE, R>();
-  static_assert(NSLOT >= 3, "ring too small");
+  constexpr int NP = pair_slots<MODE, R>();
+  static_assert(NP >= kPairs, "a tile needs four pair slots");
+  constexpr int kPre = NP - kPairs;  // pairs of tile j+1 gathered while tile j holds its four
+  constexpr int kPreUsed = kPre < kPairs ? kPre : kPairs;
   constexpr int kCols = 2 * NS * R + 4 * R;
   constexpr uint32_t kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
   constexpr int kPBytes = kTileKeys * PLayout<R>::row_bytes;  // one P^T matrix
@@ -161,8 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sQ = smem;                             // 9 k-blocks of [R x 64] bf16
   uint8_t *sP = sQ + R * CPMLA_DQK * 2;           // P^T matrices
-  uint8_t *sRing = sP + p_region_bytes<MODE, R>();
-  SparseCtrl<R> &c = *reinterpret_cast<SparseCtrl<R> *>(sRing + NSLOT * kSlotBytes);
+  uint8_t *sRope = sP + p_region_bytes<MODE, R>();  // [128 keys x 64 dims]
+  uint8_t *sRing = sRope + kKbBytes;              // NP pair slots
+  SparseCtrl<MODE, R> &c = *reinterpret_cast<SparseCtrl<MODE, R> *>(sRing + NP * kSlotBytes);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -175,12 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------ setup
   if (tid == 0) {
-    for (int s = 0; s < NSLOT; ++s) {
+    for (int s = 0; s < NP; ++s) {
       // bf16: the 128 gather threads' copies; fp8: the converter's release
       mbar_init(&c.full[s], MODE == kSparseFp8 ? 1 : 128);
       mbar_init(&c.raw[s], 128);
       mbar_init(&c.empty[s], 1);
     }
+    mbar_init(&c.rope_full, 128);
+    mbar_init(&c.rope_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.s_full[s], 1);
       mbar_init(&c.s_free[s], 128);
@@ -236,84 +237,93 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------- MMA issuer
+    // QK(0); then per tile j: [rope and first kPre pairs of QK(j+1)],
+    // PV(j), [remaining pairs of QK(j+1)]
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, R, 0, 0);
       constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
       const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
-      const uint32_t ring = smem_u32(sRing);
-      uint32_t n = 0;  // ring items consumed
+      const uint32_t ring = smem_u32(sRing), rope = smem_u32(sRope);
       bool ok = true;
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        if (i < n_tiles) {
-          const int sb = i & 1;
-          if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t dS = tmem + sb * NS * R;
-          for (int pr = 0; pr < kKItems; ++pr, ++n) {
-            const uint32_t slot = n % NSLOT;
-            if (!mbar_wait(&c.full[slot], (n / NSLOT) & 1, abort, a.status)) {
-              ok = false;
-              break;
-            }
-            // the slot was written through the generic proxy (cp.async or
-            // the converter's stores); order it before the tensor core reads
-            fence_proxy_async_smem();
-            tc_fence_after();
-            // fp8: pair pr (one 128-channel scale group) feeds accumulator pr,
-            // the rope feeds accumulator 4
-            const uint32_t d_acc = NS == 1 ? dS : dS + pr * R;
-            const int nkb = pr < 4 ? 2 : 1;
-            for (int h = 0; h < nkb; ++h) {
-              const int b = 2 * pr + h;  // k-block (8 = rope)
+      // score GEMM of pair p (k-blocks 2p, 2p+1) of tile i from its slot
+      auto qk_pair = [&](int i, int p) -> bool {
+        const uint32_t pos = 4u * i + p, slot = pos % NP;
+        if (!mbar_wait(&c.full[slot], (pos / NP) & 1, abort, a.status)) return false;
+        // written through the generic proxy (cp.async or the converter)
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t dS = tmem + (i & 1) * NS * R;
+        const uint32_t d_acc = NS == 1 ? dS : dS + p * R;  // fp8: group p
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const uint64_t da =
-                    smem_desc(ring + slot * kSlotBytes + h * kKbBytes + s * 32, 16, 1024, kSwz128);
-                const uint64_t db = smem_desc(q_base + b * (R * 128) + s * 32, 16, 1024, kSwz128);
-                const bool first = NS == 1 ? (b == 0 && s == 0) : (h == 0 && s == 0);
-                mma_bf16_ss(d_acc, da, db, id_qk, first ? 0u : 1u);
-              }
-            }
-            mma_commit(&c.empty[slot]);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint64_t da =
+                smem_desc(ring + slot * kSlotBytes + h * kKbBytes + s * 32, 16, 1024, kSwz128);
+            const uint64_t db =
+                smem_desc(q_base + (2 * p + h) * (R * 128) + s * 32, 16, 1024, kSwz128);
+            mma_bf16_ss(d_acc, da, db, id_qk, (NS != 1 && h == 0 && s == 0) ? 0u : 1u);
           }
-          if (!ok) break;
-          mma_commit(&c.s_full[sb]);
         }
-        if (i >= 1) {
-          const int j = i - 1;
-          if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int ch = 0; ch < kVItems; ++ch, ++n) {
-            const uint32_t slot = n % NSLOT;
-            if (!mbar_wait(&c.full[slot], (n / NSLOT) & 1, abort, a.status)) {
-              ok = false;
-              break;
-            }
-            fence_proxy_async_smem();
-            tc_fence_after();
+        return true;
+      };
+      // score GEMM of the rope of tile i; it starts the bf16 accumulator
+      auto qk_rope = [&](int i) -> bool {
+        if (i >= 2 && !mbar_wait(&c.s_free[i & 1], ((i >> 1) - 1) & 1, abort, a.status))
+          return false;
+        if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) return false;
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t dS = tmem + (i & 1) * NS * R;
+        const uint32_t d_acc = NS == 1 ? dS : dS + 4 * R;
 #pragma unroll
-            for (int s = 0; s < kTileKeys / 16; ++s) {
-              const uint64_t da = smem_desc(ring + slot * kSlotBytes + s * 2048, kKbBytes, 1024,
-                                            kSwz128);
-#pragma unroll
-              for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
-                const uint32_t pm = p_base + (MODE == kSparseFp8 ? (2 * ch + part) * kPBytes : 0);
-                const uint64_t db = smem_desc(pm + s * 16 * PLayout<R>::row_bytes, 8192,
-                                              8 * PLayout<R>::row_bytes, PLayout<R>::swz);
-                mma_bf16_ss(tO + ch * R, da, db, id_pv,
-                            (j > 0 || s > 0 || part > 0) ? 1u : 0u);
-              }
-            }
-            mma_commit(&c.empty[slot]);
-          }
+        for (int s = 0; s < 4; ++s) {
+          const uint64_t da = smem_desc(rope + s * 32, 16, 1024, kSwz128);
+          const uint64_t db = smem_desc(q_base + kLatKb * (R * 128) + s * 32, 16, 1024, kSwz128);
+          mma_bf16_ss(d_acc, da, db, id_qk, s == 0 ? 0u : 1u);
+        }
+        mma_commit(&c.rope_empty);
+        return true;
+      };
+      if (n_tiles > 0) {
+        ok = qk_rope(0);
+        for (int p = 0; p < kPairs && ok; ++p) ok = qk_pair(0, p);
+        if (ok) mma_commit(&c.s_full[0]);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const bool next = j + 1 < n_tiles;
+        if (next) {
+          ok = qk_rope(j + 1);
+          for (int p = 0; p < kPreUsed && ok; ++p) ok = qk_pair(j + 1, p);
           if (!ok) break;
-          mma_commit(&c.p_free);
+        }
+        // O^T += V_j^T . P_j^T from tile j's resident pairs
+        if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ch = 0; ch < kPairs; ++ch) {
+          const uint32_t slot = (4u * j + ch) % NP;
+#pragma unroll
+          for (int s = 0; s < kTileKeys / 16; ++s) {
+            const uint64_t da =
+                smem_desc(ring + slot * kSlotBytes + s * 2048, kKbBytes, 1024, kSwz128);
+#pragma unroll
+            for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
+              const uint32_t pm = p_base + (MODE == kSparseFp8 ? (2 * ch + part) * kPBytes : 0);
+              const uint64_t db = smem_desc(pm + s * 16 * PLayout<R>::row_bytes, 8192,
+                                            8 * PLayout<R>::row_bytes, PLayout<R>::swz);
+              mma_bf16_ss(tO + ch * R, da, db, id_pv, (j > 0 || s > 0 || part > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&c.empty[slot]);
+        }
+        mma_commit(&c.p_free);
+        if (next) {
+          for (int p = kPreUsed; p < kPairs && ok; ++p) ok = qk_pair(j + 1, p);
+          if (!ok) break;
+          mma_commit(&c.s_full[(j + 1) & 1]);
         }
       }
       mma_commit(&c.o_full);
@@ -325,21 +335,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 1 && warp <= 3) {
     // ---------------------------------------------------- fp8 converter
+    // pair positions in order: tile j pair p at position 4j + p
     if (MODE == kSparseFp8) {
       const int t = tid - 32;
       int seq = 0;
-      uint32_t total = 0;  // items of the whole item sequence
-      if (n_tiles > 0) total = (uint32_t)(n_tiles * (kKItems + kVItems));
-      for (uint32_t m = 0; m < total; ++m) {
-        const uint32_t slot = m % NSLOT;
-        // elected wait on the raw codes, shared by the 96 threads
+      const uint32_t total = (uint32_t)n_tiles * kPairs;
+      for (uint32_t pos = 0; pos < total; ++pos) {
+        const uint32_t slot = pos % NP;
         int *f = c.bflag[2] + (seq & 1);
         ++seq;
-        if (t == 0) *f = mbar_wait(&c.raw[slot], (m / NSLOT) & 1, abort, a.status) ? 1 : 0;
+        if (t == 0) *f = mbar_wait(&c.raw[slot], (pos / NP) & 1, abort, a.status) ? 1 : 0;
         named_bar_sync(4, 96);
         if (!*reinterpret_cast<volatile int *>(f)) break;
-        fence_proxy_async_smem();
-        if (latent_item(m, n_tiles)) convert_fp8_item(sRing + slot * kSlotBytes, t);
+        convert_fp8_item(sRing + slot * kSlotBytes, t);
         fence_proxy_async_smem();
         named_bar_sync(4, 96);
         if (t == 0) mbar_arrive(&c.full[slot]);
@@ -525,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kGatherWarp0) {
     // ---------------------------------------------------- gather producer
-    // items in the MMA issuer's order: K(0), then per i >= 1 K(i) (if any)
-    // followed by V(i-1); item n goes to slot n % NSLOT
+    // per tile: key metadata, the rope, pairs 0-3 (pair p of tile j at ring
+    // position 4j + p); each slot waits until the tensor core released it
     const int t = tid - kGatherWarp0 * 32;
     const int tpos = a.pos[row];
     const int64_t base = a.kv_start[a.req[row]];
@@ -534,88 +542,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lo = a.kv_lo ? a.kv_lo[row] : 0;
     const int hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
     int seq = 0;
-    uint32_t n = 0;
     bool ok = true;
-    for (int i = 0; i <= n_tiles && ok; ++i) {
-      for (int part = 0; part < 2 && ok; ++part) {
-        const bool is_k = part == 0;
-        if (is_k ? i >= n_tiles : i == 0) continue;
-        const int tile = is_k ? i : i - 1;
-        if (is_k) {
-          // the KV row (and fp8 scales) of key t of this tile
-          const int e = tile * kTileKeys + t;
-          const int p = e < a.k ? lst[e] : -1;
-          int src = -1;
-          if (p >= 0) {
-            if (p > tpos || base + p >= a.s_kv)
-              record_status(a.status, CPMLA_ERR_INDEX);
-            else if (p >= lo && p <= hi)
-              src = (int)(base + p);
-          }
-          float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (MODE == kSparseFp8 && src >= 0)
-            sc = __ldg(reinterpret_cast<const float4 *>(a.kv_scale) + src);
-          // the softmax of tile-2 must be done with this metadata slot
-          if (tile >= 2 && !group_wait(&c.meta_empty[tile & 1], ((tile >> 1) - 1) & 1, t, 3,
-                                       c.bflag[1], seq, abort, a.status)) {
-            ok = false;
-            break;
-          }
-          c.key_row[tile & 1][t] = src;
-          if (MODE == kSparseFp8) c.key_scale[tile & 1][t] = sc;
-          mbar_arrive(&c.meta_full[tile & 1]);
-          named_bar_sync(3, 128);
+    for (int tile = 0; tile < n_tiles && ok; ++tile) {
+      // the KV row (and fp8 scales) of key t of this tile
+      {
+        const int e = tile * kTileKeys + t;
+        const int p = e < a.k ? lst[e] : -1;
+        int src = -1;
+        if (p >= 0) {
+          if (p > tpos || base + p >= a.s_kv)
+            record_status(a.status, CPMLA_ERR_INDEX);
+          else if (p >= lo && p <= hi)
+            src = (int)(base + p);
         }
-        const int *krow = c.key_row[tile & 1];
-        const int items = is_k ? kKItems : kVItems;
-        for (int it = 0; it < items; ++it, ++n) {
-          const uint32_t slot = n % NSLOT;
-          if (n >= (uint32_t)NSLOT &&
-              !group_wait(&c.empty[slot], ((n / NSLOT) - 1) & 1, t, 3, c.bflag[1], seq, abort,
-                          a.status)) {
-            ok = false;
-            break;
+        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (MODE == kSparseFp8 && src >= 0)
+          sc = __ldg(reinterpret_cast<const float4 *>(a.kv_scale) + src);
+        // the softmax of tile-2 must be done with this metadata slot
+        if (tile >= 2 && !group_wait(&c.meta_empty[tile & 1], ((tile >> 1) - 1) & 1, t, 3,
+                                     c.bflag[1], seq, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        c.key_row[tile & 1][t] = src;
+        if (MODE == kSparseFp8) c.key_scale[tile & 1][t] = sc;
+        mbar_arrive(&c.meta_full[tile & 1]);
+        named_bar_sync(3, 128);
+      }
+      const int *krow = c.key_row[tile & 1];
+      // rope: 128 keys x 8 chunks of 16 B, a warp covering 4 keys per step
+      if (tile >= 1 &&
+          !group_wait(&c.rope_empty, (tile - 1) & 1, t, 3, c.bflag[1], seq, abort, a.status)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        const int key = st * 16 + (t >> 3), cc = t & 7;
+        const int src = krow[key];
+        const __nv_bfloat16 *gp =
+            MODE == kSparseBf16
+                ? a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + CPMLA_DV + cc * 8
+                : a.kv_rope + (int64_t)(src >= 0 ? src : 0) * CPMLA_DROPE + cc * 8;
+        cp_async_16(sRope + key * 128 + ((cc ^ (key & 7)) << 4), gp, src >= 0 ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(&c.rope_full);
+      for (int pr = 0; pr < kPairs; ++pr) {
+        const uint32_t pos = 4u * tile + pr, slot = pos % NP;
+        if (pos >= (uint32_t)NP &&
+            !group_wait(&c.empty[slot], ((pos / NP) - 1) & 1, t, 3, c.bflag[1], seq, abort,
+                        a.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t *dst = sRing + slot * kSlotBytes;
+        if (MODE == kSparseBf16) {
+          // dims [128 pr, 128 pr + 128) of 128 keys: 16 chunks per key, a
+          // warp covering 2 keys x 256 B per step; two swizzled k-blocks
+#pragma unroll
+          for (int st = 0; st < 16; ++st) {
+            const int key = st * 8 + (t >> 4), c16 = t & 15;
+            const int kb = c16 >> 3, cc = c16 & 7;
+            const int src = krow[key];
+            cp_async_16(dst + kb * kKbBytes + key * 128 + ((cc ^ (key & 7)) << 4),
+                        a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + pr * 128 + c16 * 8,
+                        src >= 0 ? 16u : 0u);
           }
-          uint8_t *dst = sRing + slot * kSlotBytes;
-          const bool rope = is_k && it == kKItems - 1;
-          if (rope) {
-            // 128 keys x 8 chunks of 16 B, a warp covering 4 keys per step
+          cp_async_arrive_noinc(&c.full[slot]);
+        } else {
+          // raw E4M3 codes of dims [128 pr, 128 pr + 128): 128 B per key,
+          // unswizzled, in the upper half of the slot
 #pragma unroll
-            for (int st = 0; st < 8; ++st) {
-              const int key = st * 16 + (t >> 3), cc = t & 7;
-              const int src = krow[key];
-              const __nv_bfloat16 *gp =
-                  MODE == kSparseBf16
-                      ? a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + CPMLA_DV + cc * 8
-                      : a.kv_rope + (int64_t)(src >= 0 ? src : 0) * CPMLA_DROPE + cc * 8;
-              cp_async_16(dst + key * 128 + ((cc ^ (key & 7)) << 4), gp, src >= 0 ? 16u : 0u);
-            }
-          } else if (MODE == kSparseBf16) {
-            // dims [128 it, 128 it + 128) of 128 keys: 16 chunks per key, a
-            // warp covering 2 keys x 256 B per step; two swizzled k-blocks
-#pragma unroll
-            for (int st = 0; st < 16; ++st) {
-              const int key = st * 8 + (t >> 4), c16 = t & 15;
-              const int kb = c16 >> 3, cc = c16 & 7;
-              const int src = krow[key];
-              cp_async_16(dst + kb * kKbBytes + key * 128 + ((cc ^ (key & 7)) << 4),
-                          a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + it * 128 + c16 * 8,
-                          src >= 0 ? 16u : 0u);
-            }
-          } else {
-            // raw E4M3 codes of dims [128 it, 128 it + 128): 128 B per key,
-            // unswizzled, in the upper half of the slot
-#pragma unroll
-            for (int st = 0; st < 8; ++st) {
-              const int key = st * 16 + (t >> 3), c8 = t & 7;
-              const int src = krow[key];
-              cp_async_16(dst + kKbBytes + key * 128 + c8 * 16,
-                          a.kv8 + (int64_t)(src >= 0 ? src : 0) * CPMLA_DV + it * 128 + c8 * 16,
-                          src >= 0 ? 16u : 0u);
-            }
+          for (int st = 0; st < 8; ++st) {
+            const int key = st * 16 + (t >> 3), c8 = t & 7;
+            const int src = krow[key];
+            cp_async_16(dst + kKbBytes + key * 128 + c8 * 16,
+                        a.kv8 + (int64_t)(src >= 0 ? src : 0) * CPMLA_DV + pr * 128 + c8 * 16,
+                        src >= 0 ? 16u : 0u);
           }
-          // the item's barrier hears from this thread once its copies land
-          cp_async_arrive_noinc(MODE == kSparseFp8 ? &c.raw[slot] : &c.full[slot]);        }
+          cp_async_arrive_noinc(&c.raw[slot]);
+        }
       }
     }
     cp_async_wait<0>();  // own copies in flight, before the CTA may exit
@@ -633,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE, int R>
 int launch_t(const AttnArgs &args, int n_items, cudaStream_t stream) {
   constexpr int smem = smem_bytes<MODE, R>();
+  static_assert(pair_slots<MODE, R>() >= kPairs, "shared memory budget");
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = mla_sparse_kernel<MODE, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
