@@ -17,11 +17,13 @@
 //     128-dv chunks [128 keys x 128 dv] -- a second read of the same
 //     L2-resident rows, so neither GEMM holds shared memory the other needs,
 //     and all 128 KB of the ring are in flight whatever the tensor core is
-//     doing.  One producer thread fills it with TMA (128-byte swizzle).
+//     doing.  Three producer threads fill it with TMA (128-byte swizzle),
+//     item n from warp 1 + n % 3: a single issuing thread caps the TMA
+//     ingress of an SM near 40 B/clk, two or more reach about twice that.
 //   * Warp 0 issues every tcgen05.mma from one thread in the order
-//     QK(0), QK(1), PV(0), QK(2), PV(1), ...; warp 1 is the producer; warps
-//     4-11 are two softmax warpgroups of 32 rows each (thread i = TMEM lane
-//     i = key i of a tile / dv i of an O^T chunk).
+//     QK(0), QK(1), PV(0), QK(2), PV(1), ...; warps 1-3 are the producers;
+//     warps 4-11 are two softmax warpgroups of 32 rows each (thread i = TMEM
+//     lane i = key i of a tile / dv i of an O^T chunk).
 //   * Tiles that lie inside every row's causal range skip the mask.
 //   * Every wait is bounded; on expiry the CTA records CPMLA_ERR_TIMEOUT,
 //     drains its copies and MMAs, and exits.
@@ -35,6 +37,7 @@ namespace {
 constexpr int kR = 64;                      // query rows per CTA (MMA N)
 constexpr int kRW = 32;                     // rows per softmax warpgroup
 constexpr int kNS = 4;                      // ring slots
+constexpr int kProducers = 3;               // TMA-issuing threads (warps 1-3)
 constexpr int kSlotBytes = 2 * kKbBytes;    // 32 KB: two k-blocks or one 128-dv chunk
 constexpr int kKPairs = 5;                  // K of a tile: k-block pairs 0-3 + rope
 constexpr int kVChunks = 4;                 // V of a tile: 128-dv chunks
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
-  if (warp == 1 && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (warp >= 1 && warp <= kProducers && lane == 0) tma_prefetch_desc(&tm_kv);
   if (tid < kR) {
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
@@ -278,11 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------- producer
+  } else if (warp >= 1 && warp <= kProducers) {
+    // ---------------------------------------------------- producers
     // the same item order as the MMA issuer: K(0), then per i >= 1
-    // K(i) (if any) followed by V(i-1)
+    // K(i) (if any) followed by V(i-1); producer w issues items n with
+    // n % kProducers == w - 1
     if (lane == 0) {
+      const uint32_t me = warp - 1;
       uint32_t n = 0;
       bool ok = true;
       for (int i = 0; i <= n_tiles && ok; ++i) {
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int y = (int)(c.tile_lo + (int64_t)tile * kTileKeys);
           const int items = is_k ? kKPairs : kVChunks;
           for (int it = 0; it < items; ++it, ++n) {
+            if (n % kProducers != me) continue;
             const uint32_t slot = n % kNS;
             if (n >= (uint32_t)kNS &&
                 !mbar_wait(&c.empty[slot], ((n / kNS) - 1) & 1, abort, a.status)) {
@@ -310,12 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        // wait for the last load issued into each slot
-        for (uint32_t s2 = 0; s2 < (uint32_t)kNS; ++s2) {
-          if (n <= s2) continue;
-          const uint32_t last = n - 1 - ((n - 1 - s2) % kNS);
-          drain_wait(&c.full[s2], (last / kNS) & 1);
-        }
+        // wait for the loads this thread issued that may still be in flight
+        for (uint32_t m = n > (uint32_t)kNS ? n - kNS : 0; m < n; ++m)
+          if (m % kProducers == me) drain_wait(&c.full[m % kNS], (m / kNS) & 1);
       }
     }
     __syncwarp();
