@@ -104,14 +104,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend=None):
+    """One process per GPU (torchrun's RANK/LOCAL_RANK/WORLD_SIZE); NCCL when
+    CUDA is present, gloo otherwise (the CPU tests of the multi-rank path)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -122,12 +129,28 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest value over the ranks (step time: the job runs at its slowest rank)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(units_per_rank, step_ms, world):
+    """Whole-job throughput of `world` replicas that each process
+    `units_per_rank` per step: all ranks' units over the max-over-ranks time."""
+    return world * units_per_rank / (step_ms * 1e-3)
+
+
+def workload_config(name, prob, world):
+    return {"workload": name, "tokens": prob.T, "heads": prob.H, "pcp": prob.P,
+            "topk": prob.topk, "kv_format": prob.kv_format,
+            "l2": "flushed between steps (512 MiB write)",
+            "parallelism": ("replicas (one full workload per GPU)" if world > 1
+                            else "single GPU, %d virtual PCP shards" % prob.P)}
 
 
 def cpu_oracle_sample(prob, target_s=12.0, max_tokens=4096, seed=0):
@@ -295,17 +318,14 @@ def main():
                "sample": "%d of %d tokens of the workload (all %d heads each), seeded, %.1f s; "
                          "%.1f tokens/s" % (n_tok, prob.T, prob.H, secs, tps)}
 
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    value = job_throughput(flops, step_ms, world) / 1e12
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/KV, N(0,1) sink; no dataset or weights)",
-        "config": {"workload": args.workload, "tokens": tokens, "heads": prob.H, "pcp": prob.P,
-                   "topk": prob.topk, "kv_format": prob.kv_format,
-                   "l2": "flushed between steps (512 MiB write)", "parallelism": "replicas"
-                   if world > 1 else "single GPU, %d virtual PCP shards" % prob.P},
-        "tokens_per_s": round(world * tokens / (step_ms * 1e-3), 1),
+        "config": workload_config(args.workload, prob, world),
+        "tokens_per_s": round(job_throughput(tokens, step_ms, world), 1),
         "attn_ms": round(attn_avg, 4), "merge_ms": round(merge_avg, 4),
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": pk["bf16"], "unit": "TFLOP/s",
@@ -353,7 +373,7 @@ def run_reference(args, world, rank):
            "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(1e3 * statistics.median(per_step), 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": args.workload}, "impl": "reference",
+           "config": workload_config(args.workload, prob, 1), "impl": "reference",
            "cpu_baseline": {"kind": "oracle", "cores": cores, "value": round(value, 6),
                             "unit": "TFLOP/s",
                             "sample": "%d tokens per step (all heads), seeded" % n_tok},
