@@ -31,6 +31,7 @@ _SIGS = {
     "cpmla_last_error": (ctypes.c_char_p, []),
     "cpmla_version": (_I, []),
     "cpmla_device_status": (_I, [_P, _I]),
+    "cpmla_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "pcp_partition_size": (_I, [_I, _I, _P, _P, _P]),
     "pcp_dualchunk_partition": (_I, [_I, _I] + [_P] * 9),
     "mla_partial_attn_dense": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I,
@@ -182,6 +183,14 @@ def device_status(clear=True):
     v = ctypes.c_int(0)
     _check(lib().cpmla_device_status(ctypes.byref(v), 1 if clear else 0))
     return v.value
+
+
+def selftest_wait_timeout(limit_ms=200, stream=None):
+    """Run a kernel whose bounded wait must give up after limit_ms; returns
+    the recorded device status (CPMLA_ERR_TIMEOUT when the machinery works)."""
+    device_status(clear=True)
+    _check(lib().cpmla_selftest_wait_timeout(int(limit_ms), _stream(stream)))
+    return device_status(clear=True)
 
 
 # ------------------------------------------------------------- the whole path

@@ -50,6 +50,37 @@ int *status_word() {
 
 }  // namespace cpmla
 
+namespace cpmla {
+namespace {
+// One thread waits, with the kernels' bounded wait, on a barrier that nothing
+// will ever arrive at; the wait gives up after limit_ns and records
+// CPMLA_ERR_TIMEOUT, exactly as a stalled pipeline stage would.
+__global__ void wait_timeout_selftest_kernel(int *status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, &abort_flag, status, limit_ns);
+}
+}  // namespace
+}  // namespace cpmla
+
+extern "C" int cpmla_selftest_wait_timeout(unsigned int limit_ms, void *stream) {
+  CPMLA_CHECK_ARG(limit_ms >= 1 && limit_ms <= 2000,
+                  "cpmla_selftest_wait_timeout: limit_ms=%u outside 1..2000", limit_ms);
+  int *status = cpmla::status_word();
+  if (!status) return cpmla::fail(CPMLA_ERR_CUDA, "cpmla_selftest_wait_timeout: status word unavailable");
+  cpmla::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, (unsigned long long)limit_ms * 1000000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cpmla::cuda_fail(e, "cpmla_selftest_wait_timeout: launch");
+  return CPMLA_OK;
+}
+
 extern "C" const char *cpmla_last_error(void) { return cpmla::t_msg; }
 
 extern "C" int cpmla_version(void) { return 100; }

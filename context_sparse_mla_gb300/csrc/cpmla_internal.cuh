@@ -70,10 +70,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up (returns
-// false) when *abort becomes non-zero or after kWaitLimitNs; in the latter
+// false) when *abort becomes non-zero or after limit_ns; in the latter
 // case it records CPMLA_ERR_TIMEOUT and raises *abort for the whole CTA.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int *status) {
+                                          int *status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -84,7 +85,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
         *abort = 1;
         return false;
       }
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         record_status(status, CPMLA_ERR_TIMEOUT);
         return false;

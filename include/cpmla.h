@@ -75,6 +75,16 @@ int cpmla_version(void);
  */
 int cpmla_device_status(int *status, int clear);
 
+/*
+ * Support entry point with no counterpart on the pages: exercises the bounded
+ * waits every kernel uses.  Launches one CTA on `stream` whose pipeline wait
+ * is on a barrier that nothing arrives at; after limit_ms (1..2000) it gives
+ * up, records CPMLA_ERR_TIMEOUT in the status word and exits normally (no
+ * trap, no fault), so the CUDA context stays usable.  Read the result with
+ * cpmla_device_status().  Errors: CPMLA_ERR_ARG, CPMLA_ERR_CUDA.
+ */
+int cpmla_selftest_wait_timeout(unsigned int limit_ms, void *stream);
+
 /* --------------------------------------------------------------------------
  * 1. DualChunkSwap partition (host)
  *

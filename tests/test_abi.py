@@ -123,3 +123,8 @@ def test_merge_argument_checks(lib):
     assert lib.lse_merge_with_sink(None, None, 5, 4, None, None, 3, None, None, None, None) == -1
     msg = lib.cpmla_last_error().decode()
     assert "NULL" in msg
+
+
+def test_selftest_limit_checked_before_the_device(lib):
+    assert lib.cpmla_selftest_wait_timeout(0, None) == cpmla.CPMLA_ERR_ARG
+    assert lib.cpmla_selftest_wait_timeout(5000, None) == cpmla.CPMLA_ERR_ARG

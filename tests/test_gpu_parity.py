@@ -202,3 +202,75 @@ def test_full_size_workload_sampled_4096_tokens(name):
     print(name, stats)
     del prob
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------ failure detection
+def test_bounded_wait_times_out_and_context_survives():
+    """A pipeline wait that is never satisfied gives up after its limit,
+    records CPMLA_ERR_TIMEOUT in the status word and exits normally; the CUDA
+    context keeps working (the small dense workload still matches)."""
+    import time
+    t0 = time.time()
+    assert cpmla.selftest_wait_timeout(200) == cpmla.CPMLA_ERR_TIMEOUT
+    assert time.time() - t0 < 30
+    assert cpmla.device_status() == 0
+    prob = synth.make_problem("dense_s256_h4_p2", device="cuda", seed=1)
+    _check_all(prob)
+
+
+# ------------------------------------------------------ more edge cases
+def test_sparse_fp8_two_head_groups():
+    prob = synth.make_problem("sparse_s128k_h16_p2_fp8", S=900, H=32, topk=256, device="cuda",
+                              seed=13)
+    _check_sample(prob, 200)
+
+
+def test_sparse_topk_width_not_a_tile_multiple():
+    prob = synth.make_problem("sparse_s32k_h32_p4", S=700, H=16, topk=300, device="cuda", seed=14)
+    _check_all(prob)
+
+
+def test_sparse_kv_split_partials_merge_to_full_attention():
+    """KV-split on the sparse path: each row's top-k keys restricted to the
+    2P chunks in turn, merged on the GPU with the sink once."""
+    S, H, P, k = 600, 16, 2, 64
+    prob = synth.make_problem("sparse_s32k_h32_p4", S=S, H=H, P=P, topk=k, device="cuda", seed=15)
+    dev = "cuda"
+    base, rem = divmod(S, 2 * P)
+    bounds, st = [], 0
+    for c in range(2 * P):
+        ln = base + (1 if c < rem else 0)
+        bounds.append((st, st + ln - 1))
+        st += ln
+    C = len(bounds)
+    rows = torch.arange(S, dtype=torch.int32, device=dev).repeat(C)
+    req = torch.zeros_like(rows)
+    lo = torch.tensor([b[0] for b in bounds], dtype=torch.int32, device=dev).repeat_interleave(S)
+    hi = torch.tensor([b[1] for b in bounds], dtype=torch.int32, device=dev).repeat_interleave(S)
+    o_part = torch.empty((C * S, H, 512), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((C * S, H), dtype=torch.float32, device=dev)
+    cpmla.mla_partial_attn_sparse(prob.q, prob.kv_start.to(dev), rows, rows.clone(), req, prob.idx,
+                                  o_part, lse_part, softmax_scale=prob.scale, kv=prob.kv,
+                                  kv_lo=lo, kv_hi=hi)
+    off = torch.arange(0, C * S + 1, C, dtype=torch.int32, device=dev)
+    contrib = (torch.arange(S, dtype=torch.int32, device=dev)[:, None]
+               + S * torch.arange(C, dtype=torch.int32, device=dev)[None, :]).reshape(-1)
+    o = torch.empty((S, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+    cpmla.lse_merge_with_sink(o_part, lse_part, contrib.contiguous(), o, lse, contrib_off=off,
+                              sink=prob.sink)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    ro, rl = pu.oracle_tokens(prob, np.arange(S))
+    pu.compare(o, lse, ro, rl)
+
+
+def test_empty_calls_are_no_ops():
+    prob = synth.make_problem("dense_s256_h4_p2", device="cuda", seed=2)
+    z = torch.zeros(0, dtype=torch.int32, device="cuda")
+    o = torch.empty((0, 4, 512), dtype=torch.float32, device="cuda")
+    l = torch.empty((0, 4), dtype=torch.float32, device="cuda")
+    cpmla.mla_partial_attn_dense(prob.q, prob.kv_start.cuda(), z, z, z, o, l,
+                                 softmax_scale=prob.scale, kv=prob.kv)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
