@@ -136,9 +136,28 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   };
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (sparse)
-    return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args,
-                         (int)n_items, st);
+  if (sparse) {
+    // one-row boxes for four-row TMA gathers: bf16 rows of 64 dims with the
+    // MMA's 128-byte swizzle (the KV, or the fp8 layout's rope), and raw fp8
+    // codes of 128 dims, unswizzled
+    CUtensorMap tm_kv, tm_rope;
+    CUresult cr2;
+    if (kv_format == CPMLA_KV_BF16) {
+      cr2 = encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, CPMLA_DQK, 2, kKbDims, 1,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+      tm_rope = tm_kv;
+    } else {
+      cr2 = encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, kv_fp8, CPMLA_DV, 1, 128, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (cr2 == CUDA_SUCCESS)
+        cr2 = encode(&tm_rope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv_rope, CPMLA_DROPE, 2,
+                     CPMLA_DROPE, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (cr2 != CUDA_SUCCESS)
+      return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr2);
+    return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args, tm_kv,
+                         tm_rope, (int)n_items, st);
+  }
   // 128-key x 64-dim tiles of the bf16 KV
   CUtensorMap tm;
   const CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, CPMLA_DQK, 2, kKbDims,

@@ -139,6 +139,10 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, int t
 
 // Launchers (one per translation unit); n_items CTAs, one work item each.
 int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st);
-int launch_sparse(int mode, int R, const AttnArgs &args, int n_items, cudaStream_t st);
+// Sparse: one-row gather maps.  bf16: tm_kv = tm_rope = the KV (box 64 x 1,
+// 128-byte swizzle).  fp8: tm_kv = the E4M3 codes (box 128 x 1, no swizzle),
+// tm_rope = the bf16 rope (box 64 x 1, 128-byte swizzle).
+int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
+                  const CUtensorMap &tm_rope, int n_items, cudaStream_t st);
 
 }  // namespace cpmla

@@ -17,13 +17,16 @@
 //     128-dv chunks [128 keys x 128 dv] -- a second read of the same
 //     L2-resident rows, so neither GEMM holds shared memory the other needs,
 //     and all 128 KB of the ring are in flight whatever the tensor core is
-//     doing.  Three producer threads fill it with TMA (128-byte swizzle),
-//     item n from warp 1 + n % 3: a single issuing thread caps the TMA
-//     ingress of an SM near 40 B/clk, two or more reach about twice that.
-//   * Warp 0 issues every tcgen05.mma from one thread in the order
-//     QK(0), QK(1), PV(0), QK(2), PV(1), ...; warps 1-3 are the producers;
-//     warps 4-11 are two softmax warpgroups of 32 rows each (thread i = TMEM
-//     lane i = key i of a tile / dv i of an O^T chunk).
+//     doing.  Two producer threads fill it with TMA (128-byte swizzle),
+//     item n from warp 2 + n % 2: a single issuing thread caps the TMA
+//     ingress of an SM near 40 B/clk, two reach about twice that.
+//   * Two threads issue the tcgen05.mma: warp 0 the score GEMMs, warp 1 the
+//     PV GEMMs, each walking the ring sequence K(0), K(1), V(0), K(2),
+//     V(1), ... and taking its own items.  One thread issues an MMA only
+//     every ~80 cycles, while the tensor core finishes an N = 64 MMA in
+//     ~48 (its shared-memory operand reads), so one issuer would leave it
+//     idle.  Warps 4-11 are two softmax warpgroups of 32 rows each (thread
+//     i = TMEM lane i = key i of a tile / dv i of an O^T chunk).
 //   * Tiles that lie inside every row's causal range skip the mask.
 //   * Every wait is bounded; on expiry the CTA records CPMLA_ERR_TIMEOUT,
 //     drains its copies and MMAs, and exits.
@@ -37,7 +40,7 @@ namespace {
 constexpr int kR = 64;                      // query rows per CTA (MMA N)
 constexpr int kRW = 32;                     // rows per softmax warpgroup
 constexpr int kNS = 4;                      // ring slots
-constexpr int kProducers = 3;               // TMA-issuing threads (warps 1-3)
+constexpr int kProducers = 2;               // TMA-issuing threads (warps 2-3)
 constexpr int kSlotBytes = 2 * kKbBytes;    // 32 KB: two k-blocks or one 128-dv chunk
 constexpr int kKPairs = 5;                  // K of a tile: k-block pairs 0-3 + rope
 constexpr int kVChunks = 4;                 // V of a tile: 128-dv chunks
@@ -45,14 +48,19 @@ constexpr int kPBytes = kTileKeys * kR * 2; // P^T, 16 KB
 constexpr uint32_t kTmemCols = 512;         // S^T x2 (128) + O^T (256)
 
 struct DenseCtrl {
-  uint64_t full[kNS];
+  // Ring item n lands on full[n % (2 kNS)]: two barriers per slot, used by
+  // alternate items of the slot.  The two MMA issuers each wait only for
+  // their own items, so one of them can wait for item n while item n - kNS
+  // (the other's) has not landed; with one barrier per slot the parity test
+  // would then pass a phase early.  Item n - 2 kNS has always landed by then.
+  uint64_t full[2 * kNS];
   uint64_t empty[kNS];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full;
   uint64_t p_free;
   uint64_t o_full;
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
   int n_tiles;
@@ -118,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&c.full[s], 1);
+      mbar_init(&c.full[kNS + s], 1);
       mbar_init(&c.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -127,13 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c.p_full, 2 * 128);
     mbar_init(&c.p_free, 1);
     mbar_init(&c.o_full, 1);
-    mbar_init(&c.drain, 1);
+    mbar_init(&c.drain[0], 1);
+    mbar_init(&c.drain[1], 1);
     c.abort = 0;
     c.need_rescale[0] = c.need_rescale[1] = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
-  if (warp >= 1 && warp <= kProducers && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (warp >= 2 && warp < 2 + kProducers && lane == 0) tma_prefetch_desc(&tm_kv);
   if (tid < kR) {
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
@@ -207,87 +217,101 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &c.abort;
 
   if (warp == 0) {
-    // ---------------------------------------------------- MMA issuer
+    // ---------------------------------------------------- score-GEMM issuer
+    // walks the ring sequence K(0), then per i >= 1 K(i) (if any) and
+    // V(i-1), consuming the K items and stepping over the V items
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, kR, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16(128, kR, 1, 1);
-      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
-      const uint32_t ring = smem_u32(sRing);
-      uint32_t n = 0;  // ring items consumed so far
+      const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
+      const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
+      uint32_t n = 0;  // ring position
       bool ok = true;
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        if (i < n_tiles) {
-          const int sb = i & 1;
-          if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        if (i >= 2) n += kVChunks;  // V(i-2) precedes K(i)
+        const int sb = i & 1;
+        if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dS = tmem + sb * kR;
+        for (int pr = 0; pr < kKPairs; ++pr, ++n) {
+          const uint32_t slot = n % kNS;
+          if (!mbar_wait(&c.full[n % (2 * kNS)], (n / (2 * kNS)) & 1, abort, a.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t dS = tmem + sb * kR;
-          for (int pr = 0; pr < kKPairs; ++pr, ++n) {
-            const uint32_t slot = n % kNS;
-            if (!mbar_wait(&c.full[slot], (n / kNS) & 1, abort, a.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const int nkb = pr < 4 ? 2 : 1;
-            for (int h = 0; h < nkb; ++h) {
-              const int b = 2 * pr + h;  // k-block (8 = rope)
+          // descriptors advance by (byte offset >> 4) in their address field
+          const uint64_t da = dr0 + ((slot * kSlotBytes) >> 4);
+          const uint64_t db = dq0 + ((2 * pr * (kR * 128)) >> 4);
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const uint64_t da =
-                    smem_desc(ring + slot * kSlotBytes + h * kKbBytes + s * 32, 16, 1024, kSwz128);
-                const uint64_t db = smem_desc(q_base + b * (kR * 128) + s * 32, 16, 1024, kSwz128);
-                mma_bf16_ss(dS, da, db, id_qk, (b | s) != 0 ? 1u : 0u);
-              }
-            }
-            mma_commit(&c.empty[slot]);
+          for (int k = 0; k < 8; ++k) {
+            if (pr == 4 && k >= 4) break;  // the rope pair has one k-block
+            const uint32_t h = k >> 2, st = k & 3;
+            mma_bf16_ss(dS, da + ((h * kKbBytes + st * 32) >> 4),
+                        db + ((h * (kR * 128) + st * 32) >> 4), id_qk,
+                        (pr | k) != 0 ? 1u : 0u);
           }
-          if (!ok) break;
-          mma_commit(&c.s_full[sb]);
+          mma_commit(&c.empty[slot]);
         }
-        if (i >= 1) {
-          const int j = i - 1;
-          if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int ch = 0; ch < kVChunks; ++ch, ++n) {
-            const uint32_t slot = n % kNS;
-            if (!mbar_wait(&c.full[slot], (n / kNS) & 1, abort, a.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int s = 0; s < kTileKeys / 16; ++s) {
-              const uint64_t da = smem_desc(ring + slot * kSlotBytes + s * 2048, kKbBytes, 1024,
-                                            kSwz128);
-              const uint64_t db = smem_desc(p_base + s * 2048, 8192, 1024, kSwz128);
-              mma_bf16_ss(tO + ch * kR, da, db, id_pv, (j > 0 || s > 0) ? 1u : 0u);
-            }
-            mma_commit(&c.empty[slot]);
-          }
-          if (!ok) break;
-          mma_commit(&c.p_free);
-        }
+        if (!ok) break;
+        mma_commit(&c.s_full[sb]);
       }
-      mma_commit(&c.o_full);
       if (!ok) {
-        mma_commit(&c.drain);
-        drain_wait(&c.drain, 0);
+        mma_commit(&c.drain[0]);
+        drain_wait(&c.drain[0], 0);
       }
     }
     __syncwarp();
-  } else if (warp >= 1 && warp <= kProducers) {
+  } else if (warp == 1) {
+    // ---------------------------------------------------- PV-GEMM issuer
+    // the same ring sequence, consuming the V items
+    if (lane == 0) {
+      constexpr uint32_t id_pv = idesc_bf16(128, kR, 1, 1);
+      const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 1024, kSwz128);
+      const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
+      uint32_t n = 0;
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        // K(0..j+1) precede V(j); V(0..j-1) too
+        n = kKPairs * (uint32_t)(j + 2 <= n_tiles ? j + 2 : n_tiles) + kVChunks * (uint32_t)j;
+        if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ch = 0; ch < kVChunks; ++ch, ++n) {
+          const uint32_t slot = n % kNS;
+          if (!mbar_wait(&c.full[n % (2 * kNS)], (n / (2 * kNS)) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = dr0 + ((slot * kSlotBytes) >> 4);
+#pragma unroll
+          for (int st = 0; st < kTileKeys / 16; ++st)
+            mma_bf16_ss(tO + ch * kR, da + ((st * 2048) >> 4), dp0 + ((st * 2048) >> 4), id_pv,
+                        (j > 0 || st > 0) ? 1u : 0u);
+          mma_commit(&c.empty[slot]);
+        }
+        if (!ok) break;
+        mma_commit(&c.p_free);
+      }
+      mma_commit(&c.o_full);
+      if (!ok) {
+        mma_commit(&c.drain[1]);
+        drain_wait(&c.drain[1], 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 2 && warp < 2 + kProducers) {
     // ---------------------------------------------------- producers
     // the same item order as the MMA issuer: K(0), then per i >= 1
     // K(i) (if any) followed by V(i-1); producer w issues items n with
-    // n % kProducers == w - 1
+    // n % kProducers == w - 2
     if (lane == 0) {
-      const uint32_t me = warp - 1;
+      const uint32_t me = warp - 2;
       uint32_t n = 0;
       bool ok = true;
       for (int i = 0; i <= n_tiles && ok; ++i) {
@@ -309,16 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K pair it: dims [128 it, 128 it + 128) (the rope pair has one
             // k-block); V chunk it: dv [128 it, 128 it + 128) -- the same boxes
             const int nkb = (is_k && it == kKPairs - 1) ? 1 : 2;
-            mbar_arrive_expect_tx(&c.full[slot], nkb * kKbBytes);
-            tma_load_2d(dst, &tm_kv, it * 128, y, &c.full[slot]);
-            if (nkb == 2) tma_load_2d(dst + kKbBytes, &tm_kv, it * 128 + 64, y, &c.full[slot]);
+            uint64_t *fb = &c.full[n % (2 * kNS)];
+            mbar_arrive_expect_tx(fb, nkb * kKbBytes);
+            tma_load_2d(dst, &tm_kv, it * 128, y, fb);
+            if (nkb == 2) tma_load_2d(dst + kKbBytes, &tm_kv, it * 128 + 64, y, fb);
           }
         }
       }
       if (!ok) {
         // wait for the loads this thread issued that may still be in flight
         for (uint32_t m = n > (uint32_t)kNS ? n - kNS : 0; m < n; ++m)
-          if (m % kProducers == me) drain_wait(&c.full[m % kNS], (m / kNS) & 1);
+          if (m % kProducers == me) drain_wait(&c.full[m % (2 * kNS)], (m / (2 * kNS)) & 1);
       }
     }
     __syncwarp();

@@ -8,10 +8,9 @@
 // fp8 KV cache.
 //
 // One CTA = one token x up to 32 heads (16 for fp8): its keys are its own, so
-// a KV tile serves only that token's heads.  The load/store-unit gather is
-// the scarce resource (its copies queue in the memory pipeline), so every key
-// row is gathered once: the latent k-blocks stay resident from the score GEMM
-// to the PV GEMM.
+// a KV tile serves only that token's heads.  The gather is the scarce
+// resource, so every key row is gathered once: the latent k-blocks stay
+// resident from the score GEMM to the PV GEMM.
 //   * Score GEMM key-major: S^T = K . Q^T, M = 128 keys, N = R rows, K = 576,
 //     into one of two TMEM buffers.  fp8 keeps one fp32 accumulator per
 //     128-channel scale group and one for the rope, so the MMA only sees exact
@@ -20,21 +19,25 @@
 //   * Shared memory holds a ring of 32 KB pair slots (two k-blocks
 //     [128 keys x 64 dims] each) and one rope slot.  Pair p of tile j sits at
 //     ring position 4j + p, so with five or more slots the first pairs of tile
-//     j+1 are gathered while tile j still holds its four.  The score GEMM of
-//     tile j+1 is issued in two parts around the PV GEMM of tile j: the rope
-//     and the pairs already in flight before it, the rest after it frees
-//     their slots.
-//   * Warps 8-11 gather: per tile they resolve the 128 keys' KV rows (and
-//     fp8 scales) into shared memory, then issue the rope and the four pairs
-//     with cp.async, each thread's completion arriving on the slot's barrier
-//     by itself (cp.async.mbarrier.arrive.noinc).  fp8 codes land raw in the
-//     upper half of their pair slot; warps 1-3 convert them in place, exactly,
-//     to bf16 and release the slot to the tensor core.
-//   * Warp 0 issues every tcgen05.mma; warps 4-7 (thread i = TMEM lane i =
-//     key i / dv i) apply the fp8 scales, mask, run the online softmax with a
-//     lazily moved base-2 reference, write P^T (fp8: per dv chunk with that
-//     chunk's scale, split into high and low bf16 parts) and finally normalise
-//     and store O and LSE.
+//     j+1 are gathered while tile j still holds its four.
+//   * Gather: warps 8-11 resolve each tile's 128 key rows (and fp8 scales)
+//     into shared memory; the rope and the pairs then arrive by TMA four-row
+//     gathers (tile::gather4), each 128-byte row landing in the MMA's
+//     128-byte-swizzled layout.  One warp issues its gathers one lane at a
+//     time, so gather throughput grows with the number of issuing warps:
+//     bf16 uses six (2-3 and 8-11), fp8 four (8-11).  fp8 codes land raw
+//     in the upper half of their pair slot; warps 2, 3 and 12 convert them
+//     in place, exactly, to bf16 and release the slot to the tensor core.
+//   * MMA issue: one thread issues an MMA only every ~80 cycles, while the
+//     tensor core finishes an N = 32 MMA in ~40 (its shared-memory operand
+//     reads), so the GEMMs have their own issuing threads: warp 0 the score
+//     GEMMs, warp 1 the PV GEMMs (fp8, whose PV issues a high and a low
+//     part per k-step: warps 1 and 13, odd and even dv chunks).
+//   * Warps 4-7 (thread i = TMEM lane i = key i / dv i) apply the fp8
+//     scales, mask, run the online softmax with a lazily moved base-2
+//     reference, write P^T (fp8: per dv chunk with that chunk's scale, split
+//     into high and low bf16 parts) and finally normalise and store O and
+//     LSE.
 //   * Every wait is bounded; on expiry the CTA records CPMLA_ERR_TIMEOUT,
 //     drains its copies and MMAs, and exits.
 #include <cmath>
@@ -45,6 +48,15 @@ namespace cpmla {
 namespace {
 
 constexpr int kGatherWarp0 = 8;
+constexpr int kConvWarp2 = 12;  // fp8: third converter warp (with 2 and 3)
+constexpr int kPv2Warp = 13;    // fp8: second PV-GEMM issuer
+
+// fp8 adds a converter warp and a second PV issuer (its PV GEMM issues two
+// MMAs, high and low part of P, per k-step)
+template <int MODE>
+__host__ __device__ constexpr int sparse_threads() {
+  return MODE == kSparseFp8 ? 448 : kThreads;
+}
 constexpr int kSlotBytes = 2 * kKbBytes;  // 32 KB pair slot
 constexpr int kPairs = 4;                 // latent k-block pairs per tile
 
@@ -63,7 +75,13 @@ template <int MODE, int R>
 struct SparseCtrl {
   uint64_t full[8];    // pair slot ready for the tensor core
   uint64_t raw[8];     // fp8: pair slot's codes landed, ready for conversion
-  uint64_t empty[8];   // pair slot released by the PV GEMM
+  // pair slot released by the PV GEMM: use u of slot s on empty[s][u % 2].
+  // Different gather warps fill consecutive uses of a slot, so a warp can
+  // wait for use u - 1 to be released before use u - 2 has been; with one
+  // barrier per slot the parity test would then pass a phase early.  Use
+  // u - 3 has always been released by then (its tile's PV GEMM precedes the
+  // softmax that frees the metadata the warp waited for).
+  uint64_t empty[8][2];
   uint64_t rope_full;
   uint64_t rope_empty;
   uint64_t s_full[2];
@@ -71,7 +89,7 @@ struct SparseCtrl {
   uint64_t p_full;
   uint64_t p_free;
   uint64_t o_full;
-  uint64_t drain;
+  uint64_t drain[3];  // per MMA-issuing thread
   uint64_t meta_full[2];   // key metadata of a tile written (gather -> softmax)
   uint64_t meta_empty[2];  // key metadata of a tile read (softmax -> gather)
   uint32_t tmem_base;
@@ -105,52 +123,82 @@ __host__ __device__ constexpr int smem_bytes() {
   return fixed_bytes<MODE, R>() + pair_slots<MODE, R>() * kSlotBytes;
 }
 
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+// Bounded wait that ignores the abort flag (used to drain own copies and MMAs).
+constexpr unsigned long long kDrainLimitNs = 20ull * 1000 * 1000;
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity,
+                                           unsigned long long limit_ns = kWaitLimitNs) {
   unsigned long long t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < kWaitLimitNs) {
+  while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < limit_ns) {
   }
+}
+
+// One lane of the warp waits (bounded); the warp takes its result.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int lane,
+                                          volatile int *abort, int *status) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
 }
 
 // In-place E4M3 -> bf16 conversion of one latent item by the 96 threads of
 // warps 1-3: the raw codes of 128 keys x 128 dims sit unswizzled in the upper
 // half of the slot (key k at 16 KB + 128 k); the result is two 128-byte-
 // swizzled k-blocks.  Unit u = (key u/8, codes 16 (u%8) ...); the eight units
-// of a key fall in one warp in the same step, so every code of the key is read
-// (one load instruction) before its bf16 row is written over it.  The
-// conversion is exact: every E4M3 value is a bf16 value.
+// of a key fall in one warp in the same step, and each batch of steps reads
+// all its codes before writing, so every code of a key is read before its
+// bf16 row is written over it.  The conversion is exact: every E4M3 value is
+// a bf16 value.
 __device__ __forceinline__ void convert_fp8_item(uint8_t *sl, int t) {
+  constexpr int kUnits = kTileKeys * 8;  // 1024 units of 16 codes
+  constexpr int kBatch = 4;              // loads in flight per thread
 #pragma unroll 1
-  for (int u = t; u < kTileKeys * 8; u += 96) {
-    const int key = u >> 3, c8 = u & 7;
-    const uint4 raw = *reinterpret_cast<const uint4 *>(sl + kKbBytes + key * 128 + c8 * 16);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[8];
+  for (int u0 = t; u0 < kUnits; u0 += 96 * kBatch) {
+    uint4 raw[kBatch];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 f0 = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
-      const float2 f1 = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
-      o[2 * q] = pack_bf16x2(f0.x, f0.y);
-      o[2 * q + 1] = pack_bf16x2(f1.x, f1.y);
+    for (int b = 0; b < kBatch; ++b) {
+      const int u = u0 + 96 * b;
+      if (u < kUnits)
+        raw[b] = *reinterpret_cast<const uint4 *>(sl + kKbBytes + (u >> 3) * 128 + (u & 7) * 16);
     }
-    // dims 16 c8 .. 16 c8 + 15 of the pair: k-block c8 / 4, chunks 2 (c8 % 4), +1
-    const int kb = c8 >> 2, cc0 = 2 * (c8 & 3);
-    uint8_t *rowp = sl + kb * kKbBytes + key * 128;
+    __syncwarp();  // the warp's codes of these keys are read before any row is written
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int u = u0 + 96 * b;
+      if (u >= kUnits) continue;
+      const int key = u >> 3, c8 = u & 7;
+      const uint32_t w[4] = {raw[b].x, raw[b].y, raw[b].z, raw[b].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f0 = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
+        const float2 f1 = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
+        o[2 * q] = pack_bf16x2(f0.x, f0.y);
+        o[2 * q + 1] = pack_bf16x2(f1.x, f1.y);
+      }
+      // dims 16 c8 .. 16 c8 + 15 of the pair: k-block c8 / 4, chunks 2 (c8 % 4), +1
+      const int kb = c8 >> 2, cc0 = 2 * (c8 & 3);
+      uint8_t *rowp = sl + kb * kKbBytes + key * 128;
+      *reinterpret_cast<uint4 *>(rowp + ((cc0 ^ (key & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4 *>(rowp + (((cc0 + 1) ^ (key & 7)) << 4)) =
+          make_uint4(o[4], o[5], o[6], o[7]);
+    }
     __syncwarp();
-    *reinterpret_cast<uint4 *>(rowp + ((cc0 ^ (key & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4 *>(rowp + (((cc0 + 1) ^ (key & 7)) << 4)) =
-        make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
 template <int MODE, int R>
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_sparse_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
+    mla_sparse_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv,
+                      const __grid_constant__ CUtensorMap tm_rope) {
   static_assert(R == 16 || R == 32, "one softmax warpgroup");
   constexpr int NS = score_accumulators<MODE>();
   constexpr int NP = pair_slots<MODE, R>();
   static_assert(NP >= kPairs, "a tile needs four pair slots");
-  constexpr int kPre = NP - kPairs;  // pairs of tile j+1 gathered while tile j holds its four
-  constexpr int kPreUsed = kPre < kPairs ? kPre : kPairs;
+  constexpr int NT = sparse_threads<MODE>();
+  constexpr int kPvIssuers = MODE == kSparseFp8 ? 2 : 1;
   constexpr int kCols = 2 * NS * R + 4 * R;
   constexpr uint32_t kTmemCols = kCols <= 128 ? 128 : (kCols <= 256 ? 256 : 512);
   constexpr int kPBytes = kTileKeys * PLayout<R>::row_bytes;  // one P^T matrix
@@ -175,12 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ setup
   if (tid == 0) {
     for (int s = 0; s < NP; ++s) {
-      // bf16: the 128 gather threads' copies; fp8: the converter's release
-      mbar_init(&c.full[s], MODE == kSparseFp8 ? 1 : 128);
-      mbar_init(&c.raw[s], 128);
-      mbar_init(&c.empty[s], 1);
+      // bf16: the four half-unit gathers of the pair; fp8: the converter's
+      // release after the two half-units of raw codes landed
+      mbar_init(&c.full[s], MODE == kSparseFp8 ? 1 : 4);
+      mbar_init(&c.raw[s], 2);
+      mbar_init(&c.empty[s][0], 1);
+      mbar_init(&c.empty[s][1], 1);
     }
-    mbar_init(&c.rope_full, 128);
+    mbar_init(&c.rope_full, 2);  // two half-units
     mbar_init(&c.rope_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.s_full[s], 1);
@@ -189,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c.meta_empty[s], 128);
     }
     mbar_init(&c.p_full, 128);
-    mbar_init(&c.p_free, 1);
-    mbar_init(&c.o_full, 1);
-    mbar_init(&c.drain, 1);
+    mbar_init(&c.p_free, kPvIssuers);
+    mbar_init(&c.o_full, kPvIssuers);
+    for (int s = 0; s < 3; ++s) mbar_init(&c.drain[s], 1);
     c.abort = 0;
     c.need_rescale = 0;
     // last non-empty slot of the token's top-k list
@@ -213,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.alpha[tid] = 1.f;
   }
   // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero padding rows)
-  for (int idx = tid; idx < R * (CPMLA_DQK / 8); idx += kThreads) {
+  for (int idx = tid; idx < R * (CPMLA_DQK / 8); idx += NT) {
     const int r = idx / (CPMLA_DQK / 8);
     const int ch = idx - r * (CPMLA_DQK / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -236,108 +286,109 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &c.abort;
 
   if (warp == 0) {
-    // ---------------------------------------------------- MMA issuer
-    // QK(0); then per tile j: [rope and first kPre pairs of QK(j+1)],
-    // PV(j), [remaining pairs of QK(j+1)]
+    // ---------------------------------------------------- score-GEMM issuer
+    // per tile: the rope (it starts the bf16 accumulator), then pairs 0-3
+    // as their slots fill
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, R, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
-      const uint32_t q_base = smem_u32(sQ), p_base = smem_u32(sP);
-      const uint32_t ring = smem_u32(sRing), rope = smem_u32(sRope);
+      // descriptors advance by (byte offset >> 4) in their address field
+      const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
+      const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
+      const uint64_t drope = smem_desc(smem_u32(sRope), 16, 1024, kSwz128);
       bool ok = true;
-      // score GEMM of pair p (k-blocks 2p, 2p+1) of tile i from its slot
-      auto qk_pair = [&](int i, int p) -> bool {
-        const uint32_t pos = 4u * i + p, slot = pos % NP;
-        if (!mbar_wait(&c.full[slot], (pos / NP) & 1, abort, a.status)) return false;
-        // written through the generic proxy (cp.async or the converter)
-        fence_proxy_async_smem();
-        tc_fence_after();
+      for (int i = 0; i < n_tiles && ok; ++i) {
         const uint32_t dS = tmem + (i & 1) * NS * R;
-        const uint32_t d_acc = NS == 1 ? dS : dS + p * R;  // fp8: group p
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint64_t da =
-                smem_desc(ring + slot * kSlotBytes + h * kKbBytes + s * 32, 16, 1024, kSwz128);
-            const uint64_t db =
-                smem_desc(q_base + (2 * p + h) * (R * 128) + s * 32, 16, 1024, kSwz128);
-            mma_bf16_ss(d_acc, da, db, id_qk, (NS != 1 && h == 0 && s == 0) ? 0u : 1u);
-          }
+        if (i >= 2 && !mbar_wait(&c.s_free[i & 1], ((i >> 1) - 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
         }
-        return true;
-      };
-      // score GEMM of the rope of tile i; it starts the bf16 accumulator
-      auto qk_rope = [&](int i) -> bool {
-        if (i >= 2 && !mbar_wait(&c.s_free[i & 1], ((i >> 1) - 1) & 1, abort, a.status))
-          return false;
-        if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) return false;
-        fence_proxy_async_smem();
+        if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        const uint32_t dS = tmem + (i & 1) * NS * R;
-        const uint32_t d_acc = NS == 1 ? dS : dS + 4 * R;
+        {
+          const uint32_t d_acc = NS == 1 ? dS : dS + 4 * R;
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const uint64_t da = smem_desc(rope + s * 32, 16, 1024, kSwz128);
-          const uint64_t db = smem_desc(q_base + kLatKb * (R * 128) + s * 32, 16, 1024, kSwz128);
-          mma_bf16_ss(d_acc, da, db, id_qk, s == 0 ? 0u : 1u);
+          for (int st = 0; st < 4; ++st)
+            mma_bf16_ss(d_acc, drope + ((st * 32) >> 4),
+                        dq0 + ((kLatKb * (R * 128) + st * 32) >> 4), id_qk, st == 0 ? 0u : 1u);
         }
         mma_commit(&c.rope_empty);
-        return true;
-      };
-      if (n_tiles > 0) {
-        ok = qk_rope(0);
-        for (int p = 0; p < kPairs && ok; ++p) ok = qk_pair(0, p);
-        if (ok) mma_commit(&c.s_full[0]);
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const bool next = j + 1 < n_tiles;
-        if (next) {
-          ok = qk_rope(j + 1);
-          for (int p = 0; p < kPreUsed && ok; ++p) ok = qk_pair(j + 1, p);
-          if (!ok) break;
+        for (int p = 0; p < kPairs; ++p) {
+          const uint32_t pos = 4u * i + p, slot = pos % NP;
+          if (!mbar_wait(&c.full[slot], (pos / NP) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          // fp8: written through the generic proxy by the converter
+          if (MODE == kSparseFp8) fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t d_acc = NS == 1 ? dS : dS + p * R;  // fp8: group p
+          const uint64_t da = dr0 + ((slot * kSlotBytes) >> 4);
+          const uint64_t db = dq0 + ((2 * p * (R * 128)) >> 4);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t h = k >> 2, st = k & 3;
+            mma_bf16_ss(d_acc, da + ((h * kKbBytes + st * 32) >> 4),
+                        db + ((h * (R * 128) + st * 32) >> 4), id_qk,
+                        (NS != 1 && k == 0) ? 0u : 1u);
+          }
         }
-        // O^T += V_j^T . P_j^T from tile j's resident pairs
+        if (!ok) break;
+        mma_commit(&c.s_full[i & 1]);
+      }
+      if (!ok) {
+        mma_commit(&c.drain[0]);
+        drain_wait(&c.drain[0], 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 || (kPvIssuers == 2 && warp == kPv2Warp)) {
+    // ---------------------------------------------------- PV-GEMM issuer(s)
+    // O^T chunk ch += V^T . P^T from tile j's resident pair ch, which is
+    // then released; with two issuers, chunk ch belongs to issuer ch % 2
+    if (lane == 0) {
+      const int me = warp == 1 ? 0 : 1;
+      constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
+      const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 8 * PLayout<R>::row_bytes, PLayout<R>::swz);
+      const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
         if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ch = 0; ch < kPairs; ++ch) {
+        for (int ch = me; ch < kPairs; ch += kPvIssuers) {
           const uint32_t slot = (4u * j + ch) % NP;
+          const uint64_t da = dr0 + ((slot * kSlotBytes) >> 4);
 #pragma unroll
-          for (int s = 0; s < kTileKeys / 16; ++s) {
-            const uint64_t da =
-                smem_desc(ring + slot * kSlotBytes + s * 2048, kKbBytes, 1024, kSwz128);
+          for (int st = 0; st < kTileKeys / 16; ++st) {
 #pragma unroll
             for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
-              const uint32_t pm = p_base + (MODE == kSparseFp8 ? (2 * ch + part) * kPBytes : 0);
-              const uint64_t db = smem_desc(pm + s * 16 * PLayout<R>::row_bytes, 8192,
-                                            8 * PLayout<R>::row_bytes, PLayout<R>::swz);
-              mma_bf16_ss(tO + ch * R, da, db, id_pv, (j > 0 || s > 0 || part > 0) ? 1u : 0u);
+              const uint32_t pm = MODE == kSparseFp8 ? (2 * ch + part) * kPBytes : 0;
+              mma_bf16_ss(tO + ch * R, da + ((st * 2048) >> 4),
+                          dp0 + ((pm + st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
+                          (j > 0 || st > 0 || part > 0) ? 1u : 0u);
             }
           }
-          mma_commit(&c.empty[slot]);
+          mma_commit(&c.empty[slot][((4u * j + ch) / NP) & 1]);
         }
         mma_commit(&c.p_free);
-        if (next) {
-          for (int p = kPreUsed; p < kPairs && ok; ++p) ok = qk_pair(j + 1, p);
-          if (!ok) break;
-          mma_commit(&c.s_full[(j + 1) & 1]);
-        }
       }
       mma_commit(&c.o_full);
       if (!ok) {
-        mma_commit(&c.drain);
-        drain_wait(&c.drain, 0);
+        mma_commit(&c.drain[1 + me]);
+        drain_wait(&c.drain[1 + me], 0);
       }
     }
     __syncwarp();
-  } else if (warp >= 1 && warp <= 3) {
+  } else if (MODE == kSparseFp8 && (warp == 2 || warp == 3 || warp == kConvWarp2)) {
     // ---------------------------------------------------- fp8 converter
     // pair positions in order: tile j pair p at position 4j + p
-    if (MODE == kSparseFp8) {
-      const int t = tid - 32;
+    {
+      const int t = (warp == kConvWarp2 ? 2 : warp - 2) * 32 + lane;
       int seq = 0;
       const uint32_t total = (uint32_t)n_tiles * kPairs;
       for (uint32_t pos = 0; pos < total; ++pos) {
@@ -531,23 +582,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= kGatherWarp0) {
-    // ---------------------------------------------------- gather producer
-    // per tile: key metadata, the rope, pairs 0-3 (pair p of tile j at ring
-    // position 4j + p); each slot waits until the tensor core released it
-    const int t = tid - kGatherWarp0 * 32;
-    const int tpos = a.pos[row];
-    const int64_t base = a.kv_start[a.req[row]];
-    const int32_t *lst = a.topk + (int64_t)a.rows[row] * a.k;
-    const int lo = a.kv_lo ? a.kv_lo[row] : 0;
-    const int hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
+  } else {
+    // ---------------------------------------------------- gather producers
+    // Warps 8-11 resolve each tile's key rows (one key per thread); every
+    // issuing warp (bf16: 2-3 and 8-11, fp8: 8-11) then gathers its share of
+    // the tile's half-units in order.  A half-unit is 64 keys x one k-block
+    // (8 KB): sixteen four-row TMA gathers, one per lane.  Unit order in a
+    // tile: rope, then the pairs (bf16: k-block 2p, 2p+1 of pair p; fp8: the
+    // raw codes of pair p); half-unit g of the launch-wide sequence belongs
+    // to issuing warp g mod the number of issuers.
+    constexpr int kIssuers = MODE == kSparseFp8 ? 4 : 6;
+    constexpr int kHalves = MODE == kSparseFp8 ? 2 * (1 + kPairs) : 2 * (1 + 2 * kPairs);
+    const bool meta = warp >= kGatherWarp0;
+    const int widx = meta ? (MODE == kSparseFp8 ? 0 : 2) + warp - kGatherWarp0 : warp - 2;
+    const int t = tid - kGatherWarp0 * 32;  // key of a tile (meta warps)
+    int tpos = 0, lo = 0, hi = 0, p_next = -1;
+    int64_t base = 0;
+    const int32_t *lst = nullptr;
+    if (meta) {
+      tpos = a.pos[row];
+      base = a.kv_start[a.req[row]];
+      lst = a.topk + (int64_t)a.rows[row] * a.k;
+      lo = a.kv_lo ? a.kv_lo[row] : 0;
+      hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
+      p_next = (n_tiles > 0 && t < a.k) ? lst[t] : -1;
+    }
     int seq = 0;
     bool ok = true;
+    // the last half-units this warp issued, drained if the CTA gives up
+    constexpr int kRec = 8;
+    uint64_t *rec_bar[kRec];
+    uint32_t rec_par[kRec];
+    int n_rec = 0;
     for (int tile = 0; tile < n_tiles && ok; ++tile) {
-      // the KV row (and fp8 scales) of key t of this tile
-      {
-        const int e = tile * kTileKeys + t;
-        const int p = e < a.k ? lst[e] : -1;
+      if (meta) {
+        // the KV row (and fp8 scales) of key t of this tile; the top-k entry
+        // of the next tile is loaded now, to be used one iteration later
+        const int p = p_next;
+        {
+          const int e = (tile + 1) * kTileKeys + t;
+          p_next = (tile + 1 < n_tiles && e < a.k) ? lst[e] : -1;
+        }
         int src = -1;
         if (p >= 0) {
           if (p > tpos || base + p >= a.s_kv)
@@ -567,64 +642,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         c.key_row[tile & 1][t] = src;
         if (MODE == kSparseFp8) c.key_scale[tile & 1][t] = sc;
         mbar_arrive(&c.meta_full[tile & 1]);
-        named_bar_sync(3, 128);
       }
-      const int *krow = c.key_row[tile & 1];
-      // rope: 128 keys x 8 chunks of 16 B, a warp covering 4 keys per step
-      if (tile >= 1 &&
-          !group_wait(&c.rope_empty, (tile - 1) & 1, t, 3, c.bflag[1], seq, abort, a.status)) {
+      if (!warp_wait(&c.meta_full[tile & 1], (tile >> 1) & 1, lane, abort, a.status)) {
         ok = false;
         break;
       }
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const int key = st * 16 + (t >> 3), cc = t & 7;
-        const int src = krow[key];
-        const __nv_bfloat16 *gp =
-            MODE == kSparseBf16
-                ? a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + CPMLA_DV + cc * 8
-                : a.kv_rope + (int64_t)(src >= 0 ? src : 0) * CPMLA_DROPE + cc * 8;
-        cp_async_16(sRope + key * 128 + ((cc ^ (key & 7)) << 4), gp, src >= 0 ? 16u : 0u);
-      }
-      cp_async_arrive_noinc(&c.rope_full);
-      for (int pr = 0; pr < kPairs; ++pr) {
-        const uint32_t pos = 4u * tile + pr, slot = pos % NP;
-        if (pos >= (uint32_t)NP &&
-            !group_wait(&c.empty[slot], ((pos / NP) - 1) & 1, t, 3, c.bflag[1], seq, abort,
-                        a.status)) {
-          ok = false;
-          break;
-        }
-        uint8_t *dst = sRing + slot * kSlotBytes;
-        if (MODE == kSparseBf16) {
-          // dims [128 pr, 128 pr + 128) of 128 keys: 16 chunks per key, a
-          // warp covering 2 keys x 256 B per step; two swizzled k-blocks
-#pragma unroll
-          for (int st = 0; st < 16; ++st) {
-            const int key = st * 8 + (t >> 4), c16 = t & 15;
-            const int kb = c16 >> 3, cc = c16 & 7;
-            const int src = krow[key];
-            cp_async_16(dst + kb * kKbBytes + key * 128 + ((cc ^ (key & 7)) << 4),
-                        a.kv + (int64_t)(src >= 0 ? src : 0) * CPMLA_DQK + pr * 128 + c16 * 8,
-                        src >= 0 ? 16u : 0u);
+      const int *krow = c.key_row[tile & 1];
+      const int first = ((widx - (tile * kHalves) % kIssuers) % kIssuers + kIssuers) % kIssuers;
+      for (int i = first; i < kHalves; i += kIssuers) {
+        const int u = i >> 1, half = i & 1;
+        uint64_t *bar;
+        uint32_t par;
+        uint8_t *dst;
+        const CUtensorMap *tm;
+        int x;
+        if (u == 0) {
+          if (tile >= 1 && !warp_wait(&c.rope_empty, (tile - 1) & 1, lane, abort, a.status)) {
+            ok = false;
+            break;
           }
-          cp_async_arrive_noinc(&c.full[slot]);
+          bar = &c.rope_full;
+          par = tile & 1;
+          dst = sRope;
+          tm = &tm_rope;
+          x = MODE == kSparseBf16 ? CPMLA_DV : 0;
         } else {
-          // raw E4M3 codes of dims [128 pr, 128 pr + 128): 128 B per key,
-          // unswizzled, in the upper half of the slot
-#pragma unroll
-          for (int st = 0; st < 8; ++st) {
-            const int key = st * 16 + (t >> 3), c8 = t & 7;
-            const int src = krow[key];
-            cp_async_16(dst + kKbBytes + key * 128 + c8 * 16,
-                        a.kv8 + (int64_t)(src >= 0 ? src : 0) * CPMLA_DV + pr * 128 + c8 * 16,
-                        src >= 0 ? 16u : 0u);
+          const int pr = MODE == kSparseBf16 ? (u - 1) >> 1 : u - 1;
+          const int kb = MODE == kSparseBf16 ? (u - 1) & 1 : 0;
+          const uint32_t pos = 4u * tile + pr, slot = pos % NP;
+          if (pos >= (uint32_t)NP &&
+              !warp_wait(&c.empty[slot][((pos / NP) - 1) & 1], (((pos / NP) - 1) >> 1) & 1, lane,
+                         abort, a.status)) {
+            ok = false;
+            break;
           }
-          cp_async_arrive_noinc(&c.raw[slot]);
+          par = (pos / NP) & 1;
+          tm = &tm_kv;
+          if (MODE == kSparseBf16) {
+            // dims [128 pr + 64 kb, +64) as one 128-byte-swizzled k-block
+            bar = &c.full[slot];
+            dst = sRing + slot * kSlotBytes + kb * kKbBytes;
+            x = pr * 128 + kb * kKbDims;
+          } else {
+            // raw E4M3 codes of dims [128 pr, 128 pr + 128): 128 B per key,
+            // unswizzled, in the upper half of the slot
+            bar = &c.raw[slot];
+            dst = sRing + slot * kSlotBytes + kKbBytes;
+            x = pr * 128;
+          }
         }
+        if (lane == 0) mbar_arrive_expect_tx(bar, kKbBytes / 2);
+        __syncwarp();
+        if (lane < 16) {
+          // keys 64 half + 4 lane .. +3; a masked key fetches row 0, which
+          // the softmax gives weight exactly 0
+          const int *kr = krow + half * 64 + 4 * lane;
+          tma_gather4(dst + half * (kKbBytes / 2) + lane * 512, tm, x, kr[0] >= 0 ? kr[0] : 0,
+                      kr[1] >= 0 ? kr[1] : 0, kr[2] >= 0 ? kr[2] : 0, kr[3] >= 0 ? kr[3] : 0,
+                      bar);
+        }
+        rec_bar[n_rec % kRec] = bar;
+        rec_par[n_rec % kRec] = par;
+        ++n_rec;
       }
     }
-    cp_async_wait<0>();  // own copies in flight, before the CTA may exit
+    if (!ok && lane == 0) {
+      // gathers of this warp that may still be landing; a phase that another
+      // warp never completed gives up after the short limit
+      for (int m = n_rec > kRec ? n_rec - kRec : 0; m < n_rec; ++m)
+        drain_wait(rec_bar[m % kRec], rec_par[m % kRec], kDrainLimitNs);
+    }
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown
@@ -637,14 +725,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE, int R>
-int launch_t(const AttnArgs &args, int n_items, cudaStream_t stream) {
+int launch_t(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &tm_rope,
+             int n_items, cudaStream_t stream) {
   constexpr int smem = smem_bytes<MODE, R>();
   static_assert(pair_slots<MODE, R>() >= kPairs, "shared memory budget");
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = mla_sparse_kernel<MODE, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: set shared memory size");
-  kern<<<n_items, kThreads, smem, stream>>>(args);
+  kern<<<n_items, sparse_threads<MODE>(), smem, stream>>>(args, tm_kv, tm_rope);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: launch");
   return CPMLA_OK;
@@ -652,10 +741,11 @@ int launch_t(const AttnArgs &args, int n_items, cudaStream_t stream) {
 
 }  // namespace
 
-int launch_sparse(int mode, int R, const AttnArgs &args, int n_items, cudaStream_t st) {
-  if (mode == kSparseFp8) return launch_t<kSparseFp8, 16>(args, n_items, st);
-  return R == 16 ? launch_t<kSparseBf16, 16>(args, n_items, st)
-                 : launch_t<kSparseBf16, 32>(args, n_items, st);
+int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
+                  const CUtensorMap &tm_rope, int n_items, cudaStream_t st) {
+  if (mode == kSparseFp8) return launch_t<kSparseFp8, 16>(args, tm_kv, tm_rope, n_items, st);
+  return R == 16 ? launch_t<kSparseBf16, 16>(args, tm_kv, tm_rope, n_items, st)
+                 : launch_t<kSparseBf16, 32>(args, tm_kv, tm_rope, n_items, st);
 }
 
 }  // namespace cpmla

@@ -146,7 +146,9 @@ int pcp_dualchunk_partition(int P, int B, const int32_t *cu_seqlens, const int32
  *   kv_format    CPMLA_KV_* (host).  Dense accepts CPMLA_KV_BF16 only.
  *   kv / kv_fp8, kv_scale, kv_rope   per kv_format (unused ones may be NULL);
  *                each 16-byte aligned
- *   s_kv         KV rows (host); every key read lies in [0, s_kv)
+ *   s_kv         KV rows (host); every key read lies in [0, s_kv).  Every
+ *                KV row must be finite: the sparse kernel reads row 0 in
+ *                place of an empty or skipped top-k slot (weight exactly 0)
  *   kv_start     int64 [B] KV row of request b's position 0
  *   rows, pos, req  int32 [n_rows] as produced by pcp_dualchunk_partition
  *   n_rows       shard rows to compute (host); 0 is a no-op
