@@ -99,11 +99,22 @@ __device__ __forceinline__ void warp_transpose_reduce(float *v, int lane) {
 }
 
 // e4m3 pair -> two floats (exact), low byte first.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+// Two E4M3 codes (low byte -> low half) -> two fp16, exactly: every E4M3
+// value, subnormals and NaN included, is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-  __half2 hh = *reinterpret_cast<__half2 *>(&h2);
-  return __half22float2(hh);
+  return h2;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 t = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&t);
+}
+
+// Two bf16 (one 32-bit word) -> two fp16, rounded to nearest.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

@@ -16,6 +16,11 @@
 //     128-channel scale group and one for the rope, so the MMA only sees exact
 //     E4M3 values.  PV GEMM: O^T += V^T . P^T, M = 128 dv x 4 chunks, N = R,
 //     K = 128 keys, reading V from the same k-blocks.
+//   * fp8 computes its latent GEMMs in fp16: E4M3 -> fp16 is one exact
+//     conversion per two codes (bf16 takes four), and P^T in fp16 keeps 11
+//     significant bits in one matrix per dv chunk.  The latent part of q is
+//     rounded to fp16 once (exact for 2^-14 <= |q| < 65504); the rope GEMM
+//     stays bf16.
 //   * Shared memory holds a ring of 32 KB pair slots (two k-blocks
 //     [128 keys x 64 dims] each) and one rope slot.  Pair p of tile j sits at
 //     ring position 4j + p, so with five or more slots the first pairs of tile
@@ -26,18 +31,18 @@
 //     128-byte-swizzled layout.  One warp issues its gathers one lane at a
 //     time, so gather throughput grows with the number of issuing warps:
 //     bf16 uses six (2-3 and 8-11), fp8 four (8-11).  fp8 codes land raw
-//     in the upper half of their pair slot; warps 2, 3 and 12 convert them
-//     in place, exactly, to bf16 and release the slot to the tensor core.
+//     in the upper half of their pair slot; warps 2, 3 and 12
+//     convert them in place, exactly, to fp16 and release the slot to the
+//     tensor core.
 //   * MMA issue: one thread issues an MMA only every ~80 cycles, while the
 //     tensor core finishes an N = 32 MMA in ~40 (its shared-memory operand
 //     reads), so the GEMMs have their own issuing threads: warp 0 the score
-//     GEMMs, warp 1 the PV GEMMs (fp8, whose PV issues a high and a low
-//     part per k-step: warps 1 and 13, odd and even dv chunks).
+//     GEMMs, warp 1 the PV GEMMs (fp8: warps 1 and 13, even and odd dv
+//     chunks, since its converter warps leave the softmax more issue slots).
 //   * Warps 4-7 (thread i = TMEM lane i = key i / dv i) apply the fp8
 //     scales, mask, run the online softmax with a lazily moved base-2
-//     reference, write P^T (fp8: per dv chunk with that chunk's scale, split
-//     into high and low bf16 parts) and finally normalise and store O and
-//     LSE.
+//     reference, write P^T (fp8: per dv chunk with that chunk's scale) and
+//     finally normalise and store O and LSE.
 //   * Every wait is bounded; on expiry the CTA records CPMLA_ERR_TIMEOUT,
 //     drains its copies and MMAs, and exits.
 #include <cmath>
@@ -48,14 +53,17 @@ namespace cpmla {
 namespace {
 
 constexpr int kGatherWarp0 = 8;
-constexpr int kConvWarp2 = 12;  // fp8: third converter warp (with 2 and 3)
 constexpr int kPv2Warp = 13;    // fp8: second PV-GEMM issuer
+constexpr int kConverters = 3;  // fp8: converter warps 2, 3, 12
 
-// fp8 adds a converter warp and a second PV issuer (its PV GEMM issues two
-// MMAs, high and low part of P, per k-step)
+// fp8 adds a converter warp and a second PV issuer
 template <int MODE>
 __host__ __device__ constexpr int sparse_threads() {
   return MODE == kSparseFp8 ? 448 : kThreads;
+}
+// converter index of a warp, or -1
+__device__ __forceinline__ int converter_index(int warp) {
+  return warp == 2 ? 0 : warp == 3 ? 1 : warp == 12 ? 2 : -1;
 }
 constexpr int kSlotBytes = 2 * kKbBytes;  // 32 KB pair slot
 constexpr int kPairs = 4;                 // latent k-block pairs per tile
@@ -65,10 +73,10 @@ __host__ __device__ constexpr int score_accumulators() {
   return MODE == kSparseFp8 ? 5 : 1;
 }
 
-// P^T matrices: one, or for fp8 one per dv chunk and part (high, low).
+// P^T matrices: one, or for fp8 one per dv chunk (that chunk's scale folded in).
 template <int MODE, int R>
 __host__ __device__ constexpr int p_region_bytes() {
-  return (MODE == kSparseFp8 ? 8 : 1) * kTileKeys * R * 2;
+  return (MODE == kSparseFp8 ? 4 : 1) * kTileKeys * R * 2;
 }
 
 template <int MODE, int R>
@@ -142,40 +150,38 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, int la
   return ok != 0;
 }
 
-// In-place E4M3 -> bf16 conversion of one latent item by the 96 threads of
-// warps 1-3: the raw codes of 128 keys x 128 dims sit unswizzled in the upper
-// half of the slot (key k at 16 KB + 128 k); the result is two 128-byte-
-// swizzled k-blocks.  Unit u = (key u/8, codes 16 (u%8) ...); the eight units
-// of a key fall in one warp in the same step, and each batch of steps reads
-// all its codes before writing, so every code of a key is read before its
-// bf16 row is written over it.  The conversion is exact: every E4M3 value is
-// a bf16 value.
-__device__ __forceinline__ void convert_fp8_item(uint8_t *sl, int t) {
+// In-place E4M3 -> fp16 conversion of one latent item by the converter
+// threads (nthr, a multiple of 32): the raw codes of 128 keys x 128 dims sit
+// unswizzled in the upper half of the slot (key k at 16 KB + 128 k); the
+// result is two 128-byte-swizzled k-blocks.  Unit u = (key u/8, codes 16
+// (u%8) ...); the eight units of a key fall in one warp in the same step,
+// and each batch of steps reads all its codes before writing, so every code
+// of a key is read before its row is written over it.  One conversion
+// instruction per two codes, and exact: every E4M3 value is an fp16 value.
+__device__ __forceinline__ void convert_fp8_item(uint8_t *sl, int t, int nthr) {
   constexpr int kUnits = kTileKeys * 8;  // 1024 units of 16 codes
   constexpr int kBatch = 4;              // loads in flight per thread
 #pragma unroll 1
-  for (int u0 = t; u0 < kUnits; u0 += 96 * kBatch) {
+  for (int u0 = t; u0 < kUnits; u0 += nthr * kBatch) {
     uint4 raw[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int u = u0 + 96 * b;
+      const int u = u0 + nthr * b;
       if (u < kUnits)
         raw[b] = *reinterpret_cast<const uint4 *>(sl + kKbBytes + (u >> 3) * 128 + (u & 7) * 16);
     }
     __syncwarp();  // the warp's codes of these keys are read before any row is written
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      const int u = u0 + 96 * b;
+      const int u = u0 + nthr * b;
       if (u >= kUnits) continue;
       const int key = u >> 3, c8 = u & 7;
       const uint32_t w[4] = {raw[b].x, raw[b].y, raw[b].z, raw[b].w};
       uint32_t o[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float2 f0 = e4m3x2_to_float2((uint16_t)(w[q] & 0xFFFFu));
-        const float2 f1 = e4m3x2_to_float2((uint16_t)(w[q] >> 16));
-        o[2 * q] = pack_bf16x2(f0.x, f0.y);
-        o[2 * q + 1] = pack_bf16x2(f1.x, f1.y);
+        o[2 * q] = e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu));
+        o[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(w[q] >> 16));
       }
       // dims 16 c8 .. 16 c8 + 15 of the pair: k-block c8 / 4, chunks 2 (c8 % 4), +1
       const int kb = c8 >> 2, cc0 = 2 * (c8 & 3);
@@ -273,6 +279,11 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
                                                 (int64_t)(h0 + r) * CPMLA_DQK) +
                 ch);
     }
+    // fp8: the latent part meets fp16 codes in the MMA, so it is fp16 too
+    // (the rope part stays bf16, against the bf16 rope)
+    if (MODE == kSparseFp8 && ch < CPMLA_DV / 8)
+      v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                     bf16x2_to_f16x2(v.w));
     const int kb = ch >> 3, cc = ch & 7;
     *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
   }
@@ -290,7 +301,8 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     // per tile: the rope (it starts the bf16 accumulator), then pairs 0-3
     // as their slots fill
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(128, R, 0, 0);
+      constexpr uint32_t id_rope = idesc_bf16(128, R, 0, 0);
+      constexpr uint32_t id_qk = MODE == kSparseFp8 ? idesc_f16(128, R, 0, 0) : id_rope;
       // descriptors advance by (byte offset >> 4) in their address field
       const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
 #pragma unroll
           for (int st = 0; st < 4; ++st)
             mma_bf16_ss(d_acc, drope + ((st * 32) >> 4),
-                        dq0 + ((kLatKb * (R * 128) + st * 32) >> 4), id_qk, st == 0 ? 0u : 1u);
+                        dq0 + ((kLatKb * (R * 128) + st * 32) >> 4), id_rope, st == 0 ? 0u : 1u);
         }
         mma_commit(&c.rope_empty);
         for (int p = 0; p < kPairs; ++p) {
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     // then released; with two issuers, chunk ch belongs to issuer ch % 2
     if (lane == 0) {
       const int me = warp == 1 ? 0 : 1;
-      constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
+      constexpr uint32_t id_pv = MODE == kSparseFp8 ? idesc_f16(128, R, 1, 1) : idesc_bf16(128, R, 1, 1);
       const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 8 * PLayout<R>::row_bytes, PLayout<R>::swz);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
       bool ok = true;
@@ -363,16 +375,12 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         for (int ch = me; ch < kPairs; ch += kPvIssuers) {
           const uint32_t slot = (4u * j + ch) % NP;
           const uint64_t da = dr0 + ((slot * kSlotBytes) >> 4);
+          const uint32_t pm = MODE == kSparseFp8 ? ch * kPBytes : 0;
 #pragma unroll
-          for (int st = 0; st < kTileKeys / 16; ++st) {
-#pragma unroll
-            for (int part = 0; part < (MODE == kSparseFp8 ? 2 : 1); ++part) {
-              const uint32_t pm = MODE == kSparseFp8 ? (2 * ch + part) * kPBytes : 0;
-              mma_bf16_ss(tO + ch * R, da + ((st * 2048) >> 4),
-                          dp0 + ((pm + st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
-                          (j > 0 || st > 0 || part > 0) ? 1u : 0u);
-            }
-          }
+          for (int st = 0; st < kTileKeys / 16; ++st)
+            mma_bf16_ss(tO + ch * R, da + ((st * 2048) >> 4),
+                        dp0 + ((pm + st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
+                        (j > 0 || st > 0) ? 1u : 0u);
           mma_commit(&c.empty[slot][((4u * j + ch) / NP) & 1]);
         }
         mma_commit(&c.p_free);
@@ -384,11 +392,11 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
       }
     }
     __syncwarp();
-  } else if (MODE == kSparseFp8 && (warp == 2 || warp == 3 || warp == kConvWarp2)) {
+  } else if (MODE == kSparseFp8 && converter_index(warp) >= 0) {
     // ---------------------------------------------------- fp8 converter
     // pair positions in order: tile j pair p at position 4j + p
     {
-      const int t = (warp == kConvWarp2 ? 2 : warp - 2) * 32 + lane;
+      const int t = converter_index(warp) * 32 + lane;
       int seq = 0;
       const uint32_t total = (uint32_t)n_tiles * kPairs;
       for (uint32_t pos = 0; pos < total; ++pos) {
@@ -396,11 +404,11 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         int *f = c.bflag[2] + (seq & 1);
         ++seq;
         if (t == 0) *f = mbar_wait(&c.raw[slot], (pos / NP) & 1, abort, a.status) ? 1 : 0;
-        named_bar_sync(4, 96);
+        named_bar_sync(4, 32 * kConverters);
         if (!*reinterpret_cast<volatile int *>(f)) break;
-        convert_fp8_item(sRing + slot * kSlotBytes, t);
+        convert_fp8_item(sRing + slot * kSlotBytes, t, 32 * kConverters);
         fence_proxy_async_smem();
-        named_bar_sync(4, 96);
+        named_bar_sync(4, 32 * kConverters);
         if (t == 0) mbar_arrive(&c.full[slot]);
       }
     }
@@ -516,21 +524,14 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         tmem_st_wait();
       }
 #pragma unroll
-      for (int m = 0; m < (NS == 1 ? 1 : 8); ++m) {
+      for (int m = 0; m < (NS == 1 ? 1 : 4); ++m) {
         uint8_t *prow = sP + m * kPBytes + t * PLayout<R>::row_bytes;
         if (NS != 1) {
-          // P^T of dv chunk m/2: p times this key's scale of channel group
-          // m/2, as a high bf16 part (m even) and the bf16 rounding of the
-          // rest (m odd); the PV GEMM adds both, so P reaches the tensor core
-          // with ~16 significant bits
+          // P^T of dv chunk m: p times this key's scale of channel group m,
+          // in fp16 (11 significant bits) against the fp16 codes
 #pragma unroll
-          for (int r = 0; r < R; r += 2) {
-            const float x0 = s[r] * ksc[m >> 1], x1 = s[r + 1] * ksc[m >> 1];
-            const uint32_t hi = pack_bf16x2(x0, x1);
-            pk[r / 2] = (m & 1) ? pack_bf16x2(x0 - __uint_as_float(hi << 16),
-                                              x1 - __uint_as_float(hi & 0xFFFF0000u))
-                                : hi;
-          }
+          for (int r = 0; r < R; r += 2)
+            pk[r / 2] = pack_f16x2(s[r] * ksc[m], s[r + 1] * ksc[m]);
         }
 #pragma unroll
         for (int ch = 0; ch < R / 8; ++ch) {

@@ -54,7 +54,10 @@ enum {
   /* kv_fp8: E4M3 latent [S_kv, 512]; kv_scale: fp32 [S_kv, 4], one scale per
    * 128 latent channels (value = e4m3 * scale); kv_rope: bf16 [S_kv, 64].
    * The pages name an fp8 MLA cache ("fp8_ds_mla") without a layout; this
-   * one is the library's own. */
+   * one is the library's own.  The sparse kernel multiplies the E4M3 codes
+   * (exactly as fp16) with the latent part of q rounded once to fp16: exact
+   * for 2^-14 <= |q| < 65504, absolute error <= 2^-25 below that range; q
+   * must stay below 65504 in magnitude.  The rope part is exact (bf16). */
   CPMLA_KV_FP8_E4M3_G128 = 1
 };
 

@@ -78,6 +78,20 @@ def test_sparse_fp8_h16_p2():
     _check_sample(prob, 300)
 
 
+def test_sparse_fp8_subnormal_codes_decode_exactly():
+    """A latent of E4M3 zeros and subnormals only (exponent field 0, values
+    m * 2^-9), scaled by 32 so they carry values up to ~0.44: a decode that
+    flushed subnormals to zero would zero V and the latent part of every
+    score."""
+    prob = synth.make_problem("sparse_s128k_h16_p2_fp8", S=400, topk=128, device="cuda", seed=17)
+    g = torch.Generator().manual_seed(17)
+    shape = tuple(prob.kv_fp8.shape)
+    codes = torch.randint(0, 8, shape, generator=g) | (torch.randint(0, 2, shape, generator=g) << 7)
+    prob.kv_fp8 = codes.to(torch.uint8).to("cuda")
+    prob.kv_scale = torch.full_like(prob.kv_scale, 32.0)
+    _check_all(prob)
+
+
 def test_sparse_varlen_h64_p8_decode():
     prob = synth.make_problem("varlen_p8_h64", prefill_lens=[2500, 1100], decode_ctx=[4100, 9000],
                               device="cuda", seed=4)
