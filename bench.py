@@ -35,7 +35,7 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload; None = not captured for the
 # current kernel).  Must be reset to None whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {}
+NCU_TRAFFIC_BYTES = {"dense_s8192_h16_p2": 163_719_680 + 213_456_128}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
@@ -179,6 +179,10 @@ def cpu_oracle_sample(prob, target_s=12.0, max_tokens=4096, seed=0):
     n0, f0, d0 = run(16)
     n = int(min(max_tokens, max(16, 16 * target_s / max(d0, 1e-3))))
     n1, f1, d1 = run(n)
+    if d1 < 0.6 * target_s and n1 < min(max_tokens, prob.T):
+        # the 16-token calibration includes thread start-up: size once more
+        n = int(min(max_tokens, n1 * target_s / max(d1, 1e-3)))
+        n1, f1, d1 = run(n)
     cores = os.cpu_count()
     try:
         cores = len(os.sched_getaffinity(0))
