@@ -105,6 +105,7 @@ struct SparseCtrl {
   int n_tiles;
   int bflag[3][2];  // elected wait results (softmax, gather, convert), alternating slots
   int need_rescale;
+  int pf_ok;  // the softmax's p_free wait succeeded (thread 0 -> its warpgroup)
   int key_row[2][kTileKeys];  // KV row per key of a tile, -1 = masked
   float4 key_scale[MODE == kSparseFp8 ? 2 : 1][MODE == kSparseFp8 ? kTileKeys : 1];
   float red[4][32];
@@ -468,26 +469,43 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         for (int r = 0; r < R; ++r)
           s[r] = (valid && r < r_valid) ? s[r] * a.scale_log2 : -INFINITY;
       }
-      {
-        float v[R];
+      // PV(j-1) must be done before P^T is overwritten or O^T rescaled:
+      // thread 0 waits, the barrier below publishes its result
+      if (t == 0)
+        c.pf_ok = (j == 0 || mbar_wait(&c.p_free, (j - 1) & 1, abort, a.status)) ? 1 : 0;
+      // The reference of a row moves only when a score passes it by more than
+      // 2^8 (always on the first tile, where it is -inf); otherwise the row
+      // maxima are not needed at all.
+      bool over = false;
 #pragma unroll
-        for (int r = 0; r < R; ++r) v[r] = s[r];
-        warp_transpose_reduce<R, true>(v, lane);
-        if (R == 32 || (lane & 1) == 0) c.red[q4][R == 32 ? lane : (lane >> 1)] = v[0];
+      for (int r = 0; r < R; ++r) over |= s[r] > c.m_ref[r] + 8.f;
+      const bool move = named_bar_or(1, 128, over);
+      if (!*reinterpret_cast<volatile int *>(&c.pf_ok)) {
+        ok = false;
+        break;
       }
-      named_bar_sync(1, 128);
-      if (t < R) {
-        const float tile_max =
-            fmaxf(fmaxf(c.red[0][t], c.red[1][t]), fmaxf(c.red[2][t], c.red[3][t]));
-        const float m_old = c.m_ref[t];
-        float m_new = m_old;
-        if (tile_max > m_old + 8.f) m_new = tile_max;  // lazy move of the reference
-        c.alpha[t] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
-        c.m_ref[t] = m_new;
-        if (j > 0 && m_new != m_old) c.need_rescale = j + 1;
+      if (move) {
+        {
+          float v[R];
+#pragma unroll
+          for (int r = 0; r < R; ++r) v[r] = s[r];
+          warp_transpose_reduce<R, true>(v, lane);
+          if (R == 32 || (lane & 1) == 0) c.red[q4][R == 32 ? lane : (lane >> 1)] = v[0];
+        }
+        named_bar_sync(1, 128);
+        if (t < R) {
+          const float tile_max =
+              fmaxf(fmaxf(c.red[0][t], c.red[1][t]), fmaxf(c.red[2][t], c.red[3][t]));
+          const float m_old = c.m_ref[t];
+          float m_new = m_old;
+          if (tile_max > m_old + 8.f) m_new = tile_max;  // lazy move of the reference
+          c.alpha[t] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
+          c.m_ref[t] = m_new;
+          if (j > 0 && m_new != m_old) c.need_rescale = j + 1;
+        }
+        named_bar_sync(1, 128);
       }
-      named_bar_sync(1, 128);
-      const bool rescale = c.need_rescale == j + 1;
+      const bool rescale = move && c.need_rescale == j + 1;
       // (s is overwritten with p)
       uint32_t pk[R / 2];
 #pragma unroll
@@ -496,15 +514,15 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         const float p0 = fast_exp2(s[r] - (m0 == -INFINITY ? 0.f : m0));
         const float p1 = fast_exp2(s[r + 1] - (m1 == -INFINITY ? 0.f : m1));
         if (NS == 1) pk[r / 2] = pack_bf16x2(p0, p1);
-        l_part[r] = l_part[r] * c.alpha[r] + p0;
-        l_part[r + 1] = l_part[r + 1] * c.alpha[r + 1] + p1;
+        if (move) {
+          l_part[r] = l_part[r] * c.alpha[r] + p0;
+          l_part[r + 1] = l_part[r + 1] * c.alpha[r + 1] + p1;
+        } else {
+          l_part[r] += p0;
+          l_part[r + 1] += p1;
+        }
         s[r] = p0;
         s[r + 1] = p1;
-      }
-      // PV(j-1) must be done before P^T is overwritten or O^T rescaled
-      if (j >= 1 && !group_wait(&c.p_free, (j - 1) & 1, t, 1, c.bflag[0], seq, abort, a.status)) {
-        ok = false;
-        break;
       }
       tc_fence_after();
       if (rescale) {
