@@ -92,6 +92,21 @@ def test_sparse_fp8_subnormal_codes_decode_exactly():
     _check_all(prob)
 
 
+@pytest.mark.parametrize("name", ["sparse_s32k_h32_p4", "sparse_s128k_h16_p2_fp8"])
+def test_sparse_max_heads(name):
+    """H = 128, the largest head count: four (bf16) or eight (fp8) head groups
+    per token, each CTA gathering the token's keys for its own group."""
+    prob = synth.make_problem(name, S=600, H=128, topk=256, device="cuda", seed=18)
+    _check_sample(prob, 96)
+
+
+def test_sparse_wide_topk():
+    """k = 8192: 64 key tiles per token, far past the 16 of the workloads."""
+    prob = synth.make_problem("sparse_s32k_h32_p4", S=9000, H=8, topk=8192, device="cuda",
+                              seed=19)
+    _check_sample(prob, 48)
+
+
 def test_sparse_varlen_h64_p8_decode():
     prob = synth.make_problem("varlen_p8_h64", prefill_lens=[2500, 1100], decode_ctx=[4100, 9000],
                               device="cuda", seed=4)
