@@ -11,18 +11,17 @@
 //     into one of two TMEM buffers, so the score GEMM of tile j+1 runs while
 //     the softmax of tile j does.  PV GEMM: O^T += V^T . P^T, M = 128 dv x 4
 //     chunks, N = 64, K = 128 keys; O^T stays in TMEM (256 columns).
-//   * One ring of four 32 KB slots streams everything the tensor core reads,
-//     in the order it reads it: K of a tile as five slots (k-block pairs of
-//     [128 keys x 64 dims], the rope k-block alone) and V of a tile as four
-//     128-dv chunks [128 keys x 128 dv] -- a second read of the same
-//     L2-resident rows, so neither GEMM holds shared memory the other needs,
-//     and all 128 KB of the ring are in flight whatever the tensor core is
-//     doing.  Two producer threads fill it with TMA (128-byte swizzle),
+//   * One ring of four 32 KB slots streams everything the tensor core reads:
+//     K of a tile as five slots (k-block pairs of [128 keys x 64 dims], the
+//     rope k-block alone) and V of a tile as four 128-dv chunks [128 keys x
+//     128 dv] -- a second read of the same L2-resident rows, so neither GEMM
+//     holds shared memory the other needs.  The sequence interleaves the two
+//     GEMMs item by item (V(t) chunk c, then K(t+2) pair c): with blocks of
+//     one GEMM's items, each issuer waited for the other's slots to turn over.  Two producer threads fill it with TMA (128-byte swizzle),
 //     item n from warp 2 + n % 2: a single issuing thread caps the TMA
 //     ingress of an SM near 40 B/clk, two reach about twice that.
 //   * Two threads issue the tcgen05.mma: warp 0 the score GEMMs, warp 1 the
-//     PV GEMMs, each walking the ring sequence K(0), K(1), V(0), K(2),
-//     V(1), ... and taking its own items.  One thread issues an MMA only
+//     PV GEMMs, each taking its own items of the ring sequence.  One thread issues an MMA only
 //     every ~80 cycles, while the tensor core finishes an N = 64 MMA in
 //     ~48 (its shared-memory operand reads), so one issuer would leave it
 //     idle.  Warps 4-11 are two softmax warpgroups of 32 rows each (thread
@@ -45,15 +44,18 @@ constexpr int kSlotBytes = 2 * kKbBytes;    // 32 KB: two k-blocks or one 128-dv
 constexpr int kKPairs = 5;                  // K of a tile: k-block pairs 0-3 + rope
 constexpr int kVChunks = 4;                 // V of a tile: 128-dv chunks
 constexpr int kPBytes = kTileKeys * kR * 2; // P^T, 16 KB
+constexpr int kFullBars = 4 * kNS;          // ring item n lands on full[n % kFullBars]
 constexpr uint32_t kTmemCols = 512;         // S^T x2 (128) + O^T (256)
 
 struct DenseCtrl {
-  // Ring item n lands on full[n % (2 kNS)]: two barriers per slot, used by
-  // alternate items of the slot.  The two MMA issuers each wait only for
-  // their own items, so one of them can wait for item n while item n - kNS
-  // (the other's) has not landed; with one barrier per slot the parity test
-  // would then pass a phase early.  Item n - 2 kNS has always landed by then.
-  uint64_t full[2 * kNS];
+  // Ring item n lands on full[n % kFullBars]: four barriers per slot, used
+  // by successive items of the slot in turn.  The two MMA issuers each wait
+  // only for their own items, so one of them can wait for item n while an
+  // earlier item of the same slot (the other's) has not landed; with too few
+  // barriers per slot the parity test would then pass a phase early.  With
+  // four, the item that last used the barrier (n - 4 kNS) has always landed
+  // by then -- checked against a randomised event model of this ring order.
+  uint64_t full[kFullBars];
   uint64_t empty[kNS];
   uint64_t s_full[2];
   uint64_t s_free[2];
@@ -101,6 +103,23 @@ __device__ __forceinline__ void row_range(const AttnArgs &a, int i, int64_t &lo,
   if (lo < 0) lo = 0;
 }
 
+// Ring order: K(0), K(1), then block t = 0, 1, ...: V(t) chunk c followed by
+// K(t+2) pair c (c = 0..3), then the rope of K(t+2); a block with no K(t+2)
+// (t >= n - 2) holds V(t) alone.  Interleaving the two GEMMs' items lets their
+// issuers run side by side instead of taking turns over the four slots.
+__device__ __forceinline__ uint32_t ring_block_base(int t, int n) {
+  const int nk = n < 2 ? n : 2;            // K(0), K(1)
+  const int nfull = n > 2 ? n - 2 : 0;     // blocks with a K part
+  const int tf = t < nfull ? t : nfull;
+  return (uint32_t)(5 * nk + 9 * tf + 4 * (t - tf));
+}
+__device__ __forceinline__ uint32_t ring_pos_k(int i, int p) {  // i < n
+  return i < 2 ? (uint32_t)(5 * i + p) : (uint32_t)(10 + 9 * (i - 2) + (p < 4 ? 2 * p + 1 : 8));
+}
+__device__ __forceinline__ uint32_t ring_pos_v(int j, int ch, int n) {
+  return ring_block_base(j, n) + (uint32_t)(j + 2 < n ? 2 * ch : ch);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mla_dense_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv) {
   extern __shared__ uint8_t smem_raw[];
@@ -125,14 +144,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ setup
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&c.full[s], 1);
-      mbar_init(&c.full[kNS + s], 1);
       mbar_init(&c.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.s_full[s], 1);
       mbar_init(&c.s_free[s], 2 * 128);
     }
+    for (int s = 0; s < kFullBars; ++s) mbar_init(&c.full[s], 1);
     mbar_init(&c.p_full, 2 * 128);
     mbar_init(&c.p_free, 1);
     mbar_init(&c.o_full, 1);
@@ -218,16 +236,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------- score-GEMM issuer
-    // walks the ring sequence K(0), then per i >= 1 K(i) (if any) and
-    // V(i-1), consuming the K items and stepping over the V items
+    // takes the K items of the ring sequence
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, kR, 0, 0);
       const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
-      uint32_t n = 0;  // ring position
       bool ok = true;
       for (int i = 0; i < n_tiles && ok; ++i) {
-        if (i >= 2) n += kVChunks;  // V(i-2) precedes K(i)
         const int sb = i & 1;
         if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
           ok = false;
@@ -235,9 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t dS = tmem + sb * kR;
-        for (int pr = 0; pr < kKPairs; ++pr, ++n) {
-          const uint32_t slot = n % kNS;
-          if (!mbar_wait(&c.full[n % (2 * kNS)], (n / (2 * kNS)) & 1, abort, a.status)) {
+        for (int pr = 0; pr < kKPairs; ++pr) {
+          const uint32_t n = ring_pos_k(i, pr), slot = n % kNS;
+          if (!mbar_wait(&c.full[n % kFullBars], (n / kFullBars) & 1, abort, a.status)) {
             ok = false;
             break;
           }
@@ -266,24 +281,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------- PV-GEMM issuer
-    // the same ring sequence, consuming the V items
+    // takes the V items of the ring sequence
     if (lane == 0) {
       constexpr uint32_t id_pv = idesc_bf16(128, kR, 1, 1);
       const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 1024, kSwz128);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
-      uint32_t n = 0;
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
-        // K(0..j+1) precede V(j); V(0..j-1) too
-        n = kKPairs * (uint32_t)(j + 2 <= n_tiles ? j + 2 : n_tiles) + kVChunks * (uint32_t)j;
         if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int ch = 0; ch < kVChunks; ++ch, ++n) {
-          const uint32_t slot = n % kNS;
-          if (!mbar_wait(&c.full[n % (2 * kNS)], (n / (2 * kNS)) & 1, abort, a.status)) {
+        for (int ch = 0; ch < kVChunks; ++ch) {
+          const uint32_t n = ring_pos_v(j, ch, n_tiles), slot = n % kNS;
+          if (!mbar_wait(&c.full[n % kFullBars], (n / kFullBars) & 1, abort, a.status)) {
             ok = false;
             break;
           }
@@ -307,43 +319,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 2 && warp < 2 + kProducers) {
     // ---------------------------------------------------- producers
-    // the same item order as the MMA issuer: K(0), then per i >= 1
-    // K(i) (if any) followed by V(i-1); producer w issues items n with
-    // n % kProducers == w - 2
+    // the ring sequence (see ring_block_base); producer w issues items n
+    // with n % kProducers == w - 2
     if (lane == 0) {
       const uint32_t me = warp - 2;
       uint32_t n = 0;
       bool ok = true;
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        for (int part = 0; part < 2 && ok; ++part) {
-          const bool is_k = part == 0;
-          if (is_k ? i >= n_tiles : i == 0) continue;
-          const int tile = is_k ? i : i - 1;
-          const int y = (int)(c.tile_lo + (int64_t)tile * kTileKeys);
-          const int items = is_k ? kKPairs : kVChunks;
-          for (int it = 0; it < items; ++it, ++n) {
-            if (n % kProducers != me) continue;
-            const uint32_t slot = n % kNS;
-            if (n >= (uint32_t)kNS &&
-                !mbar_wait(&c.empty[slot], ((n / kNS) - 1) & 1, abort, a.status)) {
-              ok = false;
-              break;
-            }
-            uint8_t *dst = sRing + slot * kSlotBytes;
-            // K pair it: dims [128 it, 128 it + 128) (the rope pair has one
-            // k-block); V chunk it: dv [128 it, 128 it + 128) -- the same boxes
-            const int nkb = (is_k && it == kKPairs - 1) ? 1 : 2;
-            uint64_t *fb = &c.full[n % (2 * kNS)];
-            mbar_arrive_expect_tx(fb, nkb * kKbBytes);
-            tma_load_2d(dst, &tm_kv, it * 128, y, fb);
-            if (nkb == 2) tma_load_2d(dst + kKbBytes, &tm_kv, it * 128 + 64, y, fb);
+      // item n: K pair / V chunk `it` of `tile` (the same [128 keys x 128]
+      // boxes; the rope pair has one k-block)
+      auto item = [&](bool is_k, int tile, int it) {
+        if (!ok) return;
+        if (n % kProducers == me) {
+          const uint32_t slot = n % kNS;
+          if (n >= (uint32_t)kNS &&
+              !mbar_wait(&c.empty[slot], ((n / kNS) - 1) & 1, abort, a.status)) {
+            ok = false;
+            return;
           }
+          const int y = (int)(c.tile_lo + (int64_t)tile * kTileKeys);
+          uint8_t *dst = sRing + slot * kSlotBytes;
+          const int nkb = (is_k && it == kKPairs - 1) ? 1 : 2;
+          uint64_t *fb = &c.full[n % kFullBars];
+          mbar_arrive_expect_tx(fb, nkb * kKbBytes);
+          tma_load_2d(dst, &tm_kv, it * 128, y, fb);
+          if (nkb == 2) tma_load_2d(dst + kKbBytes, &tm_kv, it * 128 + 64, y, fb);
         }
+        ++n;
+      };
+      for (int i = 0; i < 2 && i < n_tiles; ++i)
+        for (int p = 0; p < kKPairs; ++p) item(true, i, p);
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const bool k = t + 2 < n_tiles;
+        for (int ch = 0; ch < kVChunks; ++ch) {
+          item(false, t, ch);
+          if (k) item(true, t + 2, ch);
+        }
+        if (k) item(true, t + 2, kKPairs - 1);
       }
       if (!ok) {
         // wait for the loads this thread issued that may still be in flight
         for (uint32_t m = n > (uint32_t)kNS ? n - kNS : 0; m < n; ++m)
-          if (m % kProducers == me) drain_wait(&c.full[m % (2 * kNS)], (m / (2 * kNS)) & 1);
+          if (m % kProducers == me) drain_wait(&c.full[m % kFullBars], (m / kFullBars) & 1);
       }
     }
     __syncwarp();
