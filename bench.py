@@ -35,7 +35,7 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload; None = not captured for the
 # current kernel).  Must be reset to None whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {"dense_s8192_h16_p2": 163_719_680 + 213_456_128}
+NCU_TRAFFIC_BYTES = {"dense_s8192_h16_p2": 163_583_488 + 213_628_928}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
