@@ -35,7 +35,7 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload; None = not captured for the
 # current kernel).  Must be reset to None whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {"dense_s8192_h16_p2": 163_583_488 + 213_628_928}
+NCU_TRAFFIC_BYTES = {}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
@@ -204,6 +204,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--path", default="merged", choices=["merged", "two-launch"],
+                    help="merged: one launch, the single-partial merge with the sink in the "
+                         "attention epilogue; two-launch: partial attention, then the merge kernel")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -222,47 +225,59 @@ def main():
     prob = synth.make_problem(args.workload, device=dev, seed=args.seed)
     flops = synth.attended_keys(prob) * prob.H * FLOPS_PER_KEY_HEAD
     tokens = prob.T
-    plan = cpmla.plan_for(prob, device=dev)
+    merged = args.path == "merged"
+    plan = cpmla.plan_for(prob, device=dev)          # two-launch (partials + merge kernel)
+    plan_m = cpmla.plan_for(prob, device=dev, merged=True)
     kvk = cpmla.kv_kwargs(prob)
     o_out = torch.empty((prob.T, prob.H, 512), dtype=torch.bfloat16, device=dev)
     lse_out = torch.empty((prob.T, prob.H), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
+    def step(ev=None, two_launch=not merged):
         if ev:
             ev[0].record(stream)
-        plan.attention(prob.q, softmax_scale=prob.scale, idx=prob.idx, stream=stream, **kvk)
+        if two_launch:
+            plan.attention(prob.q, softmax_scale=prob.scale, idx=prob.idx, stream=stream, **kvk)
+        else:
+            plan_m(prob.q, softmax_scale=prob.scale, sink=prob.sink, idx=prob.idx, o_out=o_out,
+                   lse_out=lse_out, stream=stream, **kvk)
         if ev:
             ev[1].record(stream)
-        plan.merge(o_out, lse_out, sink=prob.sink, stream=stream)
+        if two_launch:
+            plan.merge(o_out, lse_out, sink=prob.sink, stream=stream)
         if ev:
             ev[2].record(stream)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
-    torch.cuda.synchronize()
-    assert cpmla.device_status() == 0
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    def timed(n, two_launch, clk=None):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step(two_launch=two_launch)
+        torch.cuda.synchronize()
+        assert cpmla.device_status() == 0
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        barrier(world)
+        torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
-        for i in range(args.steps):
+        for i in range(n):
             flush.fill_(float(i))  # evict L2 between steps (outside the events)
-            step(evs[i])
+            step(evs[i], two_launch=two_launch)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
-    barrier(world)
+        barrier(world)
+        a = [e[0].elapsed_time(e[1]) for e in evs]
+        m = [e[1].elapsed_time(e[2]) for e in evs]
+        return sum(a) / n, sum(m) / n, t_wall
+
+    # the two-launch path, for the partial-attention and merge kernels' own
+    # figures (outside the reported step when the merged path is timed)
+    tl_attn, tl_merge, _ = timed(min(args.steps, 20) if merged else 1, True)
+    with ClockSampler(local) as clk:
+        attn_avg, merge_avg, t_wall = timed(args.steps, not merged)
+    if not merged:
+        tl_attn, tl_merge = attn_avg, merge_avg
     status = cpmla.device_status()
-    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    merge_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    step_ms = sum(a + m for a, m in zip(attn_ms, merge_ms)) / args.steps
-    step_ms = max_over_ranks(step_ms, world)
-    attn_avg = sum(attn_ms) / len(attn_ms)
-    merge_avg = sum(merge_ms) / len(merge_ms)
+    step_ms = max_over_ranks(attn_avg + merge_avg, world)
 
     # ---------------- end to end through the public API with host buffers
     q_h = prob.q.cpu().pin_memory()
@@ -283,7 +298,8 @@ def main():
     d2h = o_h.numel() * 2 + lse_h.numel() * 4
 
     def e2e_step():
-        p = cpmla.PcpPrefill(prob.P, cu, qs, dec, kvs, prob.H, device=dev, topk=prob.topk)
+        p = cpmla.PcpPrefill(prob.P, cu, qs, dec, kvs, prob.H, device=dev, topk=prob.topk,
+                             merged=merged)
         q_d.copy_(q_h, non_blocking=True)
         for k in kv_d:
             kv_d[k].copy_(kv_h[k], non_blocking=True)
@@ -317,7 +333,7 @@ def main():
     n_part = plan.n_rows
     merge_bytes = n_part * prob.H * (512 * 4 + 4) + prob.T * prob.H * (512 * 2 + 4) + \
         prob.T * 4 + prob.H * 4
-    merge_gbs = merge_bytes / (merge_avg * 1e-3) / 1e9
+    merge_gbs = merge_bytes / (tl_merge * 1e-3) / 1e9
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -334,7 +350,10 @@ def main():
         "data": "synthetic (seeded N(0,1) bf16 Q/KV, N(0,1) sink; no dataset or weights)",
         "config": workload_config(args.workload, prob, world),
         "tokens_per_s": round(job_throughput(tokens, step_ms, world), 1),
+        "path": args.path,
         "attn_ms": round(attn_avg, 4), "merge_ms": round(merge_avg, 4),
+        "two_launch": {"attn_ms": round(tl_attn, 4), "merge_ms": round(tl_merge, 4),
+                       "ms_per_step": round(tl_attn + tl_merge, 4)},
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16"], 4),
@@ -343,11 +362,11 @@ def main():
                      "peak_source": pk["source"] + " burst bf16"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm"],
                            "unit": "GB/s", "frac": round(merge_gbs / pk["hbm"], 4),
-                           "bytes": merge_bytes},
+                           "bytes": merge_bytes, "kernel": "lse_merge_kernel (two-launch path)"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d + maps_bytes,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if merged else 2) * args.steps,
         "clocks": clk.summary(),
         "device_status": status,
         "wall_s_timed": round(t_wall, 3),

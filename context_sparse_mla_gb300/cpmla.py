@@ -39,6 +39,10 @@ _SIGS = {
     "mla_partial_attn_sparse": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I,
                                      _P, _P, _P, _I, _F, _P, _P, _P]),
     "lse_merge_with_sink": (_I, [_P, _P, _I64, _I, _P, _P, _I, _P, _P, _P, _P]),
+    "mla_attn_dense_merged": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I,
+                                   _P, _P, _F, _P, _I, _P, _P, _P, _P]),
+    "mla_attn_sparse_merged": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I,
+                                    _P, _P, _P, _I, _F, _P, _I, _P, _P, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -165,6 +169,30 @@ def mla_partial_attn_sparse(q, kv_start, rows, pos, req, topk_idx, o_part, lse_p
         _ptr(_dev(lse_part, torch.float32, "lse_part")), _stream(stream)))
 
 
+def mla_attn_merged(q, kv_start, rows, pos, req, owner_row, o_out, lse_out, *, softmax_scale,
+                    sink=None, topk_idx=None, kv=None, kv_fp8=None, kv_scale=None, kv_rope=None,
+                    kv_lo=None, kv_hi=None, stream=None):
+    """Attention of shard rows with the single-partial merge folded in: each
+    token's owner row writes o_out [T, H, 512] bf16 and lse_out [T, H] (sink
+    applied once to O).  Dense when topk_idx is None, else top-k sparse."""
+    fmt, s_kv = _attn_common(q, kv, kv_fp8, kv_scale, kv_rope)
+    n = rows.numel()
+    T = lse_out.shape[0]
+    common = (_ptr(q), q.stride(0), q.shape[1], fmt, _ptr(kv), _ptr(kv_fp8), _ptr(kv_scale),
+              _ptr(kv_rope), s_kv, _ptr(_dev(kv_start, torch.int64, "kv_start")),
+              _ptr(_dev(rows, torch.int32, "rows")), _ptr(_dev(pos, torch.int32, "pos")),
+              _ptr(_dev(req, torch.int32, "req")), n, _ptr(_dev(kv_lo, torch.int32, "kv_lo")),
+              _ptr(_dev(kv_hi, torch.int32, "kv_hi")))
+    tail = (float(softmax_scale), _ptr(_dev(owner_row, torch.int32, "owner_row")), T,
+            _ptr(_dev(sink, torch.float32, "sink")), _ptr(_dev(o_out, torch.bfloat16, "o_out")),
+            _ptr(_dev(lse_out, torch.float32, "lse_out")), _stream(stream))
+    if topk_idx is None:
+        _check(lib().mla_attn_dense_merged(*common, *tail))
+    else:
+        _dev(topk_idx, torch.int32, "topk_idx")
+        _check(lib().mla_attn_sparse_merged(*common, _ptr(topk_idx), topk_idx.shape[1], *tail))
+
+
 def lse_merge_with_sink(o_part, lse_part, contrib_rows, o_out, lse_out, *, contrib_off=None,
                         sink=None, stream=None):
     """Global LSE merge + sink once + global order; writes o_out [T, H, 512]
@@ -197,11 +225,13 @@ def selftest_wait_timeout(limit_ms=200, stream=None):
 class PcpPrefill:
     """The path for one batch: DualChunkSwap partition (host, once), then per
     call the partial attention of all shards in one launch and the global merge
-    in a second.  Holds the device copies of the partition maps and the fp32
-    partial buffers."""
+    in a second -- or, with merged=True, one launch whose epilogue does the
+    single-partial merge.  Holds the device copies of the partition maps and
+    the fp32 partial buffers."""
 
     def __init__(self, P, cu_seqlens, q_start_pos, is_decode, kv_start, H, *, device="cuda",
-                 topk=0):
+                 topk=0, merged=False):
+        self.merged = merged
         self.P, self.H, self.topk = P, H, topk
         part = pcp_dualchunk_partition(P, cu_seqlens, q_start_pos, is_decode)
         self.part = part
@@ -212,8 +242,11 @@ class PcpPrefill:
         self.kv_start = torch.as_tensor(np.asarray(kv_start, np.int64)).to(dev)
         self.n_rows = len(part["rows"])
         self.T = len(part["owner_row"])
-        self.o_part = torch.empty((self.n_rows, H, DV), dtype=torch.float32, device=dev)
-        self.lse_part = torch.empty((self.n_rows, H), dtype=torch.float32, device=dev)
+        # the fp32 partials exist only for the two-launch path
+        self.o_part = self.lse_part = None
+        if not merged:
+            self.o_part = torch.empty((self.n_rows, H, DV), dtype=torch.float32, device=dev)
+            self.lse_part = torch.empty((self.n_rows, H), dtype=torch.float32, device=dev)
 
     def attention(self, q, *, softmax_scale, idx=None, stream=None, **kv):
         if self.topk:
@@ -234,6 +267,11 @@ class PcpPrefill:
             o_out = torch.empty((self.T, self.H, DV), dtype=torch.bfloat16, device=q.device)
         if lse_out is None:
             lse_out = torch.empty((self.T, self.H), dtype=torch.float32, device=q.device)
+        if self.merged:
+            mla_attn_merged(q, self.kv_start, self.rows, self.pos, self.req, self.owner_row,
+                            o_out, lse_out, softmax_scale=softmax_scale, sink=sink,
+                            topk_idx=idx if self.topk else None, stream=stream, **kv)
+            return o_out, lse_out
         self.attention(q, softmax_scale=softmax_scale, idx=idx, stream=stream, **kv)
         self.merge(o_out, lse_out, sink=sink, stream=stream)
         return o_out, lse_out
@@ -246,7 +284,7 @@ def kv_kwargs(prob):
     return dict(kv_fp8=prob.kv_fp8, kv_scale=prob.kv_scale, kv_rope=prob.kv_rope)
 
 
-def plan_for(prob, device="cuda"):
+def plan_for(prob, device="cuda", merged=False):
     return PcpPrefill(prob.P, prob.cu_seqlens.numpy(), prob.q_start_pos.numpy(),
                       prob.is_decode.numpy(), prob.kv_start.numpy(), prob.H, device=device,
-                      topk=prob.topk)
+                      topk=prob.topk, merged=merged)

@@ -6,8 +6,12 @@
 // "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
 // MegaMoE", "Implementation summary" (O and LSE over the row's keys, no sink),
 // over the full latent KV ("[Core] Add MRV2 virtual-batch PCP for MLA",
-// "DualChunkSwap partitioning").  The kernels live in attn_dense.cu and
-// attn_sparse.cu.
+// "DualChunkSwap partitioning").  mla_attn_dense_merged /
+// mla_attn_sparse_merged run the same kernels with the merge folded into
+// their epilogue for the query-partitioned case, where every token has one
+// partial: its owner row applies the sink once and writes bf16 O and the LSE
+// in global token order, the merge kernel's arithmetic for one partial.  The
+// kernels live in attn_dense.cu and attn_sparse.cu.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -41,8 +45,11 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
                int64_t s_kv, const int64_t *kv_start, const int32_t *rows, const int32_t *pos,
                const int32_t *req, int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
                const int32_t *topk, int k, float softmax_scale, float *o_part, float *lse_part,
+               const int32_t *owner_row, int T, const float *sink, void *o_out, float *lse_out,
                void *stream) {
-  const char *fn = sparse ? "mla_partial_attn_sparse" : "mla_partial_attn_dense";
+  const bool merged = o_out != nullptr;
+  const char *fn = merged ? (sparse ? "mla_attn_sparse_merged" : "mla_attn_dense_merged")
+                          : (sparse ? "mla_partial_attn_sparse" : "mla_partial_attn_dense");
   CPMLA_CHECK_ARG(n_rows >= 0, "%s: n_rows=%d < 0", fn, n_rows);
   CPMLA_CHECK_ARG(H >= 1 && H <= 128 && (H <= 64 || H % 64 == 0),
                   "%s: H=%d unsupported (1..64, or a multiple of 64 up to 128)", fn, H);
@@ -58,9 +65,13 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   CPMLA_CHECK_ARG(s_kv >= 1 && s_kv <= INT32_MAX, "%s: s_kv=%lld outside 1..2^31-1", fn,
                   (long long)s_kv);
   if (sparse) CPMLA_CHECK_ARG(k >= 1 && k <= 65536, "%s: k=%d outside 1..65536", fn, k);
+  if (merged) CPMLA_CHECK_ARG(T >= 0, "%s: T=%d < 0", fn, T);
   if (n_rows == 0) return CPMLA_OK;
-  CPMLA_CHECK_ARG(q && kv_start && rows && pos && req && o_part && lse_part,
-                  "%s: a required pointer is NULL", fn);
+  CPMLA_CHECK_ARG(q && kv_start && rows && pos && req, "%s: a required pointer is NULL", fn);
+  if (merged)
+    CPMLA_CHECK_ARG(owner_row && lse_out, "%s: owner_row, o_out and lse_out are required", fn);
+  else
+    CPMLA_CHECK_ARG(o_part && lse_part, "%s: o_part and lse_part are required", fn);
   CPMLA_CHECK_ARG(((uintptr_t)q & 15) == 0, "%s: q must be 16-byte aligned", fn);
   if (kv_format == CPMLA_KV_BF16) {
     CPMLA_CHECK_ARG(kv != nullptr && ((uintptr_t)kv & 15) == 0,
@@ -97,6 +108,11 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   args.scale_log2 = softmax_scale * 1.4426950408889634f;
   args.o_part = o_part;
   args.lse_part = lse_part;
+  args.o_out = static_cast<__nv_bfloat16 *>(o_out);
+  args.lse_out = lse_out;
+  args.sink = sink;
+  args.owner_row = owner_row;
+  args.T = T;
   args.status = status;
 
   // rows per CTA: dense packs G tokens x Hc heads into R = 64; sparse keeps one
@@ -178,7 +194,8 @@ extern "C" int mla_partial_attn_dense(const void *q, int64_t q_token_stride, int
                                       void *stream) {
   return cpmla::attn_entry(false, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope,
                            s_kv, kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, nullptr, 0,
-                           softmax_scale, o_part, lse_part, stream);
+                           softmax_scale, o_part, lse_part, nullptr, 0, nullptr, nullptr,
+                           nullptr, stream);
 }
 
 extern "C" int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, int H,
@@ -191,5 +208,36 @@ extern "C" int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, in
                                        float *o_part, float *lse_part, void *stream) {
   return cpmla::attn_entry(true, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope,
                            s_kv, kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, topk_idx, k,
-                           softmax_scale, o_part, lse_part, stream);
+                           softmax_scale, o_part, lse_part, nullptr, 0, nullptr, nullptr,
+                           nullptr, stream);
+}
+
+extern "C" int mla_attn_dense_merged(const void *q, int64_t q_token_stride, int H, int kv_format,
+                                     const void *kv, const void *kv_fp8, const float *kv_scale,
+                                     const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                                     const int32_t *rows, const int32_t *pos, const int32_t *req,
+                                     int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+                                     float softmax_scale, const int32_t *owner_row, int T,
+                                     const float *sink, void *o_out, float *lse_out,
+                                     void *stream) {
+  using namespace cpmla;
+  CPMLA_CHECK_ARG(n_rows == 0 || o_out, "mla_attn_dense_merged: o_out is NULL");
+  return attn_entry(false, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope, s_kv,
+                    kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, nullptr, 0, softmax_scale,
+                    nullptr, nullptr, owner_row, T, sink, o_out, lse_out, stream);
+}
+
+extern "C" int mla_attn_sparse_merged(const void *q, int64_t q_token_stride, int H, int kv_format,
+                                      const void *kv, const void *kv_fp8, const float *kv_scale,
+                                      const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                                      const int32_t *rows, const int32_t *pos, const int32_t *req,
+                                      int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+                                      const int32_t *topk_idx, int k, float softmax_scale,
+                                      const int32_t *owner_row, int T, const float *sink,
+                                      void *o_out, float *lse_out, void *stream) {
+  using namespace cpmla;
+  CPMLA_CHECK_ARG(n_rows == 0 || o_out, "mla_attn_sparse_merged: o_out is NULL");
+  return attn_entry(true, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope, s_kv,
+                    kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, topk_idx, k, softmax_scale,
+                    nullptr, nullptr, owner_row, T, sink, o_out, lse_out, stream);
 }

@@ -46,11 +46,27 @@ struct AttnArgs {
   float scale_log2;  // softmax scale * log2(e)
   float *o_part;
   float *lse_part;
+  // Merged output (o_out non-NULL): instead of o_part / lse_part, the owner
+  // row of each global token writes its (single) partial merged with the sink
+  // straight to the token's place in o_out (bf16) and lse_out.
+  __nv_bfloat16 *o_out;
+  float *lse_out;
+  const float *sink;         // [H] or NULL
+  const int32_t *owner_row;  // [T]: the shard row that owns global token g
+  int T;
   int hc;         // heads per CTA
   int g;          // tokens per CTA
   int n_hgroups;  // H / hc
   int *status;
 };
+
+// Sink factor of a merged row with natural-log LSE L: 1 / (1 + e^(sink - L)),
+// written as the merge kernel computes it, so that a fused epilogue and the
+// partial + merge path give the same bits; 0 for an empty row.
+__device__ __forceinline__ float sink_factor(const float *sink, int h, float L) {
+  if (L == -INFINITY) return 0.f;
+  return sink ? 1.f / (1.f + expf(sink[h] - L)) : 1.f;
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

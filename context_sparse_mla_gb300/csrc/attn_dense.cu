@@ -77,6 +77,8 @@ struct DenseCtrl {
   float alpha[kR];
   float lse[kR];
   float inv_l[kR];
+  float sfac[kR];  // merged output: sink factor per row
+  int gtok[kR];    // merged output: global token a row writes, or -1
 };
 
 constexpr int kQBytes = kR * CPMLA_DQK * 2;
@@ -120,6 +122,9 @@ __device__ __forceinline__ uint32_t ring_pos_v(int j, int ch, int n) {
   return ring_block_base(j, n) + (uint32_t)(j + 2 < n ? 2 * ch : ch);
 }
 
+// MERGED: the epilogue writes each owned token's merged result
+// (AttnArgs::o_out) instead of the partial (o_part / lse_part).
+template <bool MERGED>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_dense_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv) {
   extern __shared__ uint8_t smem_raw[];
@@ -223,6 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     c.rlo[tid] = rlo;
+    // merged: the global token row tid writes, if its shard row owns it (a
+    // decode row is computed once per shard, owned by one)
+    int gt = -1;
+    if (MERGED && tid < r_valid && row0 + l < a.n_rows) {
+      const int g = a.rows[row0 + l];
+      if (g < 0 || g >= a.T)
+        record_status(a.status, CPMLA_ERR_INDEX);
+      else if (a.owner_row[g] == row0 + l)
+        gt = g;
+    }
+    c.gtok[tid] = gt;
     c.rhi[tid] = rhi;
   }
   fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
@@ -484,7 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r < r_valid) {
           const int lrow = r / a.hc, hh = r - lrow * a.hc;
           const int i = row0 + lrow;
-          if (i < a.n_rows) a.lse_part[(int64_t)i * a.H + h0 + hh] = c.lse[r];
+          if (!MERGED) {
+            if (i < a.n_rows) a.lse_part[(int64_t)i * a.H + h0 + hh] = c.lse[r];
+          } else if (c.gtok[r] >= 0) {
+            c.sfac[r] = sink_factor(a.sink, h0 + hh, c.lse[r]);
+            a.lse_out[(int64_t)c.gtok[r] * a.H + h0 + hh] = c.lse[r];
+          }
         }
       }
       named_bar_sync(bar_id, 128);
@@ -506,9 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r < r_valid) {
               const int lrow = r / a.hc, hh = r - lrow * a.hc;
               const int i = row0 + lrow;
-              if (i < a.n_rows)
-                a.o_part[((int64_t)i * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
-                    o[x] * c.inv_l[r];
+              if (!MERGED) {
+                if (i < a.n_rows)
+                  a.o_part[((int64_t)i * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
+                      o[x] * c.inv_l[r];
+              } else if (c.gtok[r] >= 0) {
+                a.o_out[((int64_t)c.gtok[r] * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
+                    __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
+              }
             }
           }
         }
@@ -528,10 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st) {
-  cudaError_t e =
-      cudaFuncSetAttribute(mla_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto kern = args.o_out ? mla_dense_kernel<true> : mla_dense_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return cuda_fail(e, "dense attention: set shared memory size");
-  mla_dense_kernel<<<n_items, kThreads, kSmem, st>>>(args, tm_kv);
+  kern<<<n_items, kThreads, kSmem, st>>>(args, tm_kv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dense attention: launch");
   return CPMLA_OK;

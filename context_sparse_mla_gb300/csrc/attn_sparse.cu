@@ -113,6 +113,8 @@ struct SparseCtrl {
   float alpha[R];
   float lse[R];
   float inv_l[R];
+  float sfac[R];  // merged output: sink factor per head row
+  int gtok;       // merged output: the global token this CTA writes, or -1
 };
 
 template <int MODE, int R>
@@ -196,7 +198,9 @@ __device__ __forceinline__ void convert_fp8_item(uint8_t *sl, int t, int nthr) {
   }
 }
 
-template <int MODE, int R>
+// MERGED: the epilogue writes the token's merged result (AttnArgs::o_out)
+// instead of the partial (o_part / lse_part).
+template <int MODE, int R, bool MERGED>
 __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     mla_sparse_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv,
                       const __grid_constant__ CUtensorMap tm_rope) {
@@ -262,6 +266,16 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         }
     }
     c.n_tiles = (last + kTileKeys) / kTileKeys;
+    // merged: the global token this CTA writes, if its row owns it (a
+    // decode row is computed once per shard, owned by one)
+    c.gtok = -1;
+    if (MERGED && row < a.n_rows) {
+      const int g = a.rows[row];
+      if (g < 0 || g >= a.T)
+        record_status(a.status, CPMLA_ERR_INDEX);
+      else if (a.owner_row[g] == row)
+        c.gtok = g;
+    }
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
@@ -576,7 +590,14 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         const bool empty = !(l > 0.f) || m == -INFINITY;
         c.lse[t] = empty ? -INFINITY : (m + __log2f(l)) * 0.69314718055994530942f;
         c.inv_l[t] = empty ? 0.f : 1.f / l;
-        if (t < r_valid && row < a.n_rows) a.lse_part[(int64_t)row * a.H + h0 + t] = c.lse[t];
+        if (t < r_valid && row < a.n_rows) {
+          if (!MERGED) {
+            a.lse_part[(int64_t)row * a.H + h0 + t] = c.lse[t];
+          } else if (c.gtok >= 0) {
+            c.sfac[t] = sink_factor(a.sink, h0 + t, c.lse[t]);
+            a.lse_out[(int64_t)c.gtok * a.H + h0 + t] = c.lse[t];
+          }
+        }
       }
       named_bar_sync(1, 128);
 #pragma unroll 1
@@ -591,12 +612,22 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
 #pragma unroll
             for (int x = 0; x < 16; ++x) o[x] = 0.f;
           }
+          if (!MERGED) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int r = cc * 16 + x;
-            if (r < r_valid && row < a.n_rows)
-              a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
-                  o[x] * c.inv_l[r];
+            for (int x = 0; x < 16; ++x) {
+              const int r = cc * 16 + x;
+              if (r < r_valid && row < a.n_rows)
+                a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
+                    o[x] * c.inv_l[r];
+            }
+          } else if (c.gtok >= 0) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const int r = cc * 16 + x;
+              if (r < r_valid)
+                a.o_out[((int64_t)c.gtok * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
+                    __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
+            }
           }
         }
       }
@@ -743,13 +774,13 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
   }
 }
 
-template <int MODE, int R>
+template <int MODE, int R, bool MERGED>
 int launch_t(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &tm_rope,
              int n_items, cudaStream_t stream) {
   constexpr int smem = smem_bytes<MODE, R>();
   static_assert(pair_slots<MODE, R>() >= kPairs, "shared memory budget");
   static_assert(smem <= 232448, "shared memory budget");
-  auto kern = mla_sparse_kernel<MODE, R>;
+  auto kern = mla_sparse_kernel<MODE, R, MERGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: set shared memory size");
   kern<<<n_items, sparse_threads<MODE>(), smem, stream>>>(args, tm_kv, tm_rope);
@@ -762,9 +793,15 @@ int launch_t(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &
 
 int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
                   const CUtensorMap &tm_rope, int n_items, cudaStream_t st) {
-  if (mode == kSparseFp8) return launch_t<kSparseFp8, 16>(args, tm_kv, tm_rope, n_items, st);
-  return R == 16 ? launch_t<kSparseBf16, 16>(args, tm_kv, tm_rope, n_items, st)
-                 : launch_t<kSparseBf16, 32>(args, tm_kv, tm_rope, n_items, st);
+  if (args.o_out) {
+    if (mode == kSparseFp8)
+      return launch_t<kSparseFp8, 16, true>(args, tm_kv, tm_rope, n_items, st);
+    return R == 16 ? launch_t<kSparseBf16, 16, true>(args, tm_kv, tm_rope, n_items, st)
+                   : launch_t<kSparseBf16, 32, true>(args, tm_kv, tm_rope, n_items, st);
+  }
+  if (mode == kSparseFp8) return launch_t<kSparseFp8, 16, false>(args, tm_kv, tm_rope, n_items, st);
+  return R == 16 ? launch_t<kSparseBf16, 16, false>(args, tm_kv, tm_rope, n_items, st)
+                 : launch_t<kSparseBf16, 32, false>(args, tm_kv, tm_rope, n_items, st);
 }
 
 }  // namespace cpmla

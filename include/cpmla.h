@@ -180,6 +180,52 @@ int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, int H, int kv
                             float *lse_part, void *stream);
 
 /* --------------------------------------------------------------------------
+ * 2b. Partial attention with the merge folded in (query-partitioned path)
+ *
+ * The pages merge per-shard partials globally, apply the sink once and
+ * restore global order ("[DeepSeekV4][PCP] ...", "Implementation summary";
+ * "[Core] Add MRV2 virtual-batch PCP for MLA", "DualChunkSwap partitioning").
+ * When every global token has exactly one partial -- its owner shard row, as
+ * after pcp_dualchunk_partition -- that merge is the identity on O and LSE, so
+ * these entry points (the library's own fusion; the pages have no
+ * counterpart) run the partial-attention kernels of section 2 and let the
+ * owner row write the final result directly:
+ *   lse_out[g,h] = LSE of the row (natural log, without the sink)
+ *   o_out[g,h,:] = bf16( (O_row[h,:]) * 1 / (1 + exp(sink[h] - LSE)) )
+ * with the same fp32 operations, in the same order, as the partial
+ * attention followed by lse_merge_with_sink; an empty row gives O = 0,
+ * LSE = -inf.  Replica rows that do not own their token (decode rows in
+ * shards other than their owner) write nothing.
+ *
+ * Arguments as in section 2, without o_part / lse_part, plus (device unless
+ * noted):
+ *   owner_row  int32 [T]: the shard row that owns global token g (the
+ *              partition's owner_row); rows[i] = g is written only when
+ *              owner_row[g] == i
+ *   T          global tokens (host)
+ *   sink       fp32 [H] or NULL
+ *   o_out      bf16 [T, H, 512] output; lse_out fp32 [T, H] output
+ * Errors: as section 2.  A shard row whose token lies outside [0, T) is
+ * skipped and recorded as CPMLA_ERR_INDEX in the status word.
+ * ------------------------------------------------------------------------ */
+int mla_attn_dense_merged(const void *q, int64_t q_token_stride, int H, int kv_format,
+                          const void *kv, const void *kv_fp8, const float *kv_scale,
+                          const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                          const int32_t *rows, const int32_t *pos, const int32_t *req,
+                          int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+                          float softmax_scale, const int32_t *owner_row, int T, const float *sink,
+                          void *o_out, float *lse_out, void *stream);
+
+int mla_attn_sparse_merged(const void *q, int64_t q_token_stride, int H, int kv_format,
+                           const void *kv, const void *kv_fp8, const float *kv_scale,
+                           const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                           const int32_t *rows, const int32_t *pos, const int32_t *req,
+                           int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+                           const int32_t *topk_idx, int k, float softmax_scale,
+                           const int32_t *owner_row, int T, const float *sink, void *o_out,
+                           float *lse_out, void *stream);
+
+/* --------------------------------------------------------------------------
  * 3. Global LSE merge + attention sink once + restore to global order (device)
  *
  * "[DeepSeekV4][PCP] ...", "Implementation summary" (merge LSE/output

@@ -36,7 +36,7 @@ def _declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert {"pcp_dualchunk_partition", "mla_partial_attn_dense", "mla_partial_attn_sparse",
-            "lse_merge_with_sink"} <= set(names)
+            "lse_merge_with_sink", "mla_attn_dense_merged", "mla_attn_sparse_merged"} <= set(names)
     h = ctypes.CDLL(cpmla.LIB_PATH)
     for n in names:
         assert hasattr(h, n), n
@@ -115,6 +115,18 @@ def test_attention_argument_checks_fail_before_the_device(lib):
     rc = lib.mla_partial_attn_sparse(None, 576, 1, 0, None, None, None, None, 16, None, None, None,
                                      None, 1, None, None, None, 0, 0.07, None, None, None)
     assert rc == cpmla.CPMLA_ERR_ARG  # k = 0
+
+
+def test_merged_attention_argument_checks(lib):
+    base = [None, 576 * 4, 4, 0, None, None, None, None, 16, None, None, None, None]
+    # empty is a no-op; otherwise o_out, owner_row and lse_out are required
+    assert lib.mla_attn_dense_merged(*base, 0, None, None, 0.07, None, 0, None, None, None,
+                                     None) == cpmla.CPMLA_OK
+    assert lib.mla_attn_dense_merged(*base, 1, None, None, 0.07, None, 4, None, None, None,
+                                     None) == cpmla.CPMLA_ERR_ARG
+    assert b"o_out" in lib.cpmla_last_error()
+    assert lib.mla_attn_sparse_merged(*base, 1, None, None, None, 8, 0.07, None, -1, None, None,
+                                      None, None) == cpmla.CPMLA_ERR_ARG
 
 
 def test_merge_argument_checks(lib):

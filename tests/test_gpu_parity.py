@@ -185,6 +185,44 @@ def test_kv_split_partials_merge_to_full_attention():
     pu.compare(o, lse, ro, rl)
 
 
+# ------------------------------------------------ merge folded into attention
+@pytest.mark.parametrize("name,kw", [
+    ("dense_s8192_h16_p2", dict(S=1000, seed=21)),
+    ("sparse_s32k_h32_p4", dict(S=3000, seed=22)),
+    ("sparse_s128k_h16_p2_fp8", dict(S=2600, seed=23)),
+    ("varlen_p8_h64", dict(prefill_lens=[2500, 1100], decode_ctx=[4100, 9000], seed=24)),
+])
+def test_merged_epilogue_matches_oracle_and_two_launch_path(name, kw):
+    """The single-partial merge folded into the attention epilogue: parity
+    with the oracle, and the same bits as partial attention + merge kernel
+    (both compute (O / l) * 1 / (1 + e^(sink - L)) in fp32 in that order)."""
+    prob = synth.make_problem(name, device="cuda", **kw)
+    o2, l2, _ = pu.run_path(prob)
+    plan = cpmla.plan_for(prob, merged=True)
+    o1, l1 = plan(prob.q, softmax_scale=prob.scale, sink=prob.sink, idx=prob.idx,
+                  **cpmla.kv_kwargs(prob))
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+    toks = pu.sample_tokens(prob, 256)
+    ro, rl = pu.oracle_tokens(prob, toks)
+    ti = torch.as_tensor(toks, device=o1.device)
+    pu.compare(o1[ti], l1[ti], ro, rl)
+
+
+def test_merged_epilogue_full_size_dense_sampled():
+    prob = synth.make_problem("dense_s8192_h16_p2", device="cuda", seed=0)
+    plan = cpmla.plan_for(prob, merged=True)
+    o, lse = plan(prob.q, softmax_scale=prob.scale, sink=prob.sink, **cpmla.kv_kwargs(prob))
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    toks = pu.sample_tokens(prob, 4096)
+    ro, rl = pu.oracle_tokens(prob, toks)
+    ti = torch.as_tensor(toks, device=o.device)
+    pu.compare(o[ti], lse[ti], ro, rl)
+
+
 def test_merge_kernel_against_oracle_merge():
     rng = np.random.default_rng(17)
     n_part, H, T = 300, 6, 120
