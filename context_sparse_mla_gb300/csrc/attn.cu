@@ -68,8 +68,10 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   if (merged) CPMLA_CHECK_ARG(T >= 0, "%s: T=%d < 0", fn, T);
   if (n_rows == 0) return CPMLA_OK;
   CPMLA_CHECK_ARG(q && kv_start && rows && pos && req, "%s: a required pointer is NULL", fn);
-  if (merged)
+  if (merged) {
     CPMLA_CHECK_ARG(owner_row && lse_out, "%s: owner_row, o_out and lse_out are required", fn);
+    CPMLA_CHECK_ARG(((uintptr_t)o_out & 15) == 0, "%s: o_out must be 16-byte aligned", fn);
+  }
   else
     CPMLA_CHECK_ARG(o_part && lse_part, "%s: o_part and lse_part are required", fn);
   CPMLA_CHECK_ARG(((uintptr_t)q & 15) == 0, "%s: q must be 16-byte aligned", fn);

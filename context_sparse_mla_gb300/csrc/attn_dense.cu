@@ -532,12 +532,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                   a.o_part[((int64_t)i * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
                       o[x] * c.inv_l[r];
               } else if (c.gtok[r] >= 0) {
-                a.o_out[((int64_t)c.gtok[r] * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
+                // merged: stage bf16 rows [row][dv] in the idle ring, stored below
+                reinterpret_cast<__nv_bfloat16 *>(sRing)[r * CPMLA_DV + ch * 128 + t] =
                     __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
               }
             }
           }
         }
+      }
+    }
+    if (MERGED) {
+      // each owned token's hc heads are one contiguous span of o_out: one
+      // bulk copy per token from the staged rows, once both warpgroups are
+      // here (both always arrive, also after an abort, which skips the copy)
+      fence_proxy_async_smem();
+      named_bar_sync(3, 2 * 128);
+      if (wg == 0 && t == 0 && !*abort) {
+        for (int lrow = 0; lrow < a.g && lrow * a.hc < r_valid; ++lrow) {
+          const int g = c.gtok[lrow * a.hc];
+          if (g < 0) continue;
+          bulk_store_s2g(a.o_out + ((int64_t)g * a.H + h0) * CPMLA_DV,
+                         sRing + (size_t)lrow * a.hc * CPMLA_DV * 2,
+                         (uint32_t)a.hc * CPMLA_DV * 2);
+        }
+        bulk_commit();
+        bulk_wait_read();
       }
     }
   }

@@ -621,14 +621,27 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
                     o[x] * c.inv_l[r];
             }
           } else if (c.gtok >= 0) {
+            // merged: stage bf16 rows [head][dv] in the idle ring, stored below
+            __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(sRing);
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
               const int r = cc * 16 + x;
-              if (r < r_valid)
-                a.o_out[((int64_t)c.gtok * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
-                    __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
+              stage[r * CPMLA_DV + ch * 128 + t] =
+                  __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
             }
           }
+        }
+      }
+      if (MERGED && c.gtok >= 0) {
+        // the token's heads h0 .. h0 + r_valid - 1 are one contiguous span of
+        // o_out: one bulk copy from the staged rows
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (t == 0) {
+          bulk_store_s2g(a.o_out + ((int64_t)c.gtok * a.H + h0) * CPMLA_DV, sRing,
+                         (uint32_t)r_valid * CPMLA_DV * 2);
+          bulk_commit();
+          bulk_wait_read();
         }
       }
     }

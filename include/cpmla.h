@@ -204,7 +204,8 @@ int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, int H, int kv
  *              owner_row[g] == i
  *   T          global tokens (host)
  *   sink       fp32 [H] or NULL
- *   o_out      bf16 [T, H, 512] output; lse_out fp32 [T, H] output
+ *   o_out      bf16 [T, H, 512] output, 16-byte aligned (each owned token's
+ *              rows are written by bulk copies); lse_out fp32 [T, H] output
  * Errors: as section 2.  A shard row whose token lies outside [0, T) is
  * skipped and recorded as CPMLA_ERR_INDEX in the status word.
  * ------------------------------------------------------------------------ */
