@@ -79,6 +79,9 @@ struct DenseCtrl {
   float inv_l[kR];
   float sfac[kR];  // merged output: sink factor per row
   int gtok[kR];    // merged output: global token a row writes, or -1
+  int64_t tlo[kR], thi[kR];  // per token of the item: valid keys (global rows, inclusive)
+  int ttok[kR];              // per token: global token, -1 past the last shard row
+  int town[kR];              // merged, per token: the token if its row owns it, else -1
 };
 
 constexpr int kQBytes = kR * CPMLA_DQK * 2;
@@ -171,29 +174,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
   }
-  // Q rows -> K-major, 128-byte-swizzled k-blocks (zero rows for padding)
-  for (int idx = tid; idx < kR * (CPMLA_DQK / 8); idx += kThreads) {
-    const int r = idx / (CPMLA_DQK / 8);
-    const int ch = idx - r * (CPMLA_DQK / 8);
-    const int l = r / a.hc, hh = r - l * a.hc;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < r_valid && row0 + l < a.n_rows) {
-      const int64_t gtok = a.rows[row0 + l];
-      v = __ldg(reinterpret_cast<const uint4 *>(a.q + gtok * a.q_stride +
-                                                (int64_t)(h0 + hh) * CPMLA_DQK) +
-                ch);
+  // Per token l of the item (one thread each, in parallel): its global token,
+  // valid key range and, merged, whether its shard row owns the token.  The
+  // loads form short dependent chains, so they run side by side, not in one
+  // thread's loop.
+  if (tid < a.g) {
+    const int i = row0 + tid;
+    int64_t lo = 1, hi = 0;  // empty
+    int tok = -1, own = -1;
+    if (i < a.n_rows) {
+      row_range(a, i, lo, hi);
+      if (a.pos[i] + a.kv_start[a.req[i]] > a.s_kv - 1) record_status(a.status, CPMLA_ERR_INDEX);
+      tok = a.rows[i];
+      if (MERGED) {
+        if (tok < 0 || tok >= a.T)
+          record_status(a.status, CPMLA_ERR_INDEX);
+        else if (a.owner_row[tok] == i)
+          own = tok;
+      }
     }
-    const int kb = ch >> 3, cc = ch & 7;
-    *reinterpret_cast<uint4 *>(sQ + kb * (kR * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+    c.tlo[tid] = lo;
+    c.thi[tid] = hi;
+    c.ttok[tid] = tok;
+    c.town[tid] = own;
+  }
+  __syncthreads();
+  // Q rows -> K-major, 128-byte-swizzled k-blocks (zero rows for padding):
+  // every thread issues all its loads before its first store
+  {
+    constexpr int kPer = kR * (CPMLA_DQK / 8) / kThreads;  // 12 16-byte chunks per thread
+    static_assert(kPer * kThreads == kR * (CPMLA_DQK / 8), "Q chunks per thread");
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kThreads;
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      const int l = r / a.hc, hh = r - l * a.hc;
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (r < r_valid && c.ttok[l] >= 0)
+        v[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + (int64_t)c.ttok[l] * a.q_stride +
+                                                     (int64_t)(h0 + hh) * CPMLA_DQK) +
+                     ch);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kThreads;
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      const int kb = ch >> 3, cc = ch & 7;
+      *reinterpret_cast<uint4 *>(sQ + kb * (kR * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v[k];
+    }
   }
   // key range of the item and the tiles that need no mask
   if (tid == 0) {
     int64_t lo_min = INT64_MAX, hi_max = INT64_MIN, lo_max = INT64_MIN, hi_min = INT64_MAX;
     for (int l = 0; l < a.g && row0 + l < a.n_rows; ++l) {
-      int64_t lo, hi;
-      row_range(a, row0 + l, lo, hi);
-      if (a.pos[row0 + l] + a.kv_start[a.req[row0 + l]] > a.s_kv - 1)
-        record_status(a.status, CPMLA_ERR_INDEX);
+      const int64_t lo = c.tlo[l], hi = c.thi[l];
       lo_max = lo > lo_max ? lo : lo_max;
       hi_min = hi < hi_min ? hi : hi_min;
       if (hi >= lo) {
@@ -219,27 +256,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < kR) {
     const int l = tid / a.hc;
     int rlo = 1, rhi = 0;  // empty
+    int gt = -1;
     if (tid < r_valid && row0 + l < a.n_rows) {
-      int64_t lo, hi;
-      row_range(a, row0 + l, lo, hi);
+      const int64_t lo = c.tlo[l], hi = c.thi[l];
       if (hi >= lo) {
         rlo = (int)(lo - c.tile_lo);
         rhi = (int)(hi - c.tile_lo);
       }
+      gt = c.town[l];  // merged: the global token row tid writes, if owned
     }
     c.rlo[tid] = rlo;
-    // merged: the global token row tid writes, if its shard row owns it (a
-    // decode row is computed once per shard, owned by one)
-    int gt = -1;
-    if (MERGED && tid < r_valid && row0 + l < a.n_rows) {
-      const int g = a.rows[row0 + l];
-      if (g < 0 || g >= a.T)
-        record_status(a.status, CPMLA_ERR_INDEX);
-      else if (a.owner_row[g] == row0 + l)
-        gt = g;
-    }
-    c.gtok[tid] = gt;
     c.rhi[tid] = rhi;
+    c.gtok[tid] = gt;
   }
   fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
   tc_fence_before();

@@ -283,24 +283,39 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
   }
-  // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero padding rows)
-  for (int idx = tid; idx < R * (CPMLA_DQK / 8); idx += NT) {
-    const int r = idx / (CPMLA_DQK / 8);
-    const int ch = idx - r * (CPMLA_DQK / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < r_valid && row < a.n_rows) {
-      const int64_t gtok = a.rows[row];
-      v = __ldg(reinterpret_cast<const uint4 *>(a.q + gtok * a.q_stride +
-                                                (int64_t)(h0 + r) * CPMLA_DQK) +
-                ch);
+  // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero padding
+  // rows): the token once, then every thread's loads before its stores
+  {
+    const int64_t gq = row < a.n_rows ? (int64_t)a.rows[row] : -1;
+    constexpr int kChunks = R * (CPMLA_DQK / 8);
+    constexpr int kPer = (kChunks + NT - 1) / NT;
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * NT;
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (idx < kChunks && r < r_valid && gq >= 0)
+        v[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + gq * a.q_stride +
+                                                     (int64_t)(h0 + r) * CPMLA_DQK) +
+                     ch);
     }
-    // fp8: the latent part meets fp16 codes in the MMA, so it is fp16 too
-    // (the rope part stays bf16, against the bf16 rope)
-    if (MODE == kSparseFp8 && ch < CPMLA_DV / 8)
-      v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                     bf16x2_to_f16x2(v.w));
-    const int kb = ch >> 3, cc = ch & 7;
-    *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * NT;
+      if (idx >= kChunks) continue;
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      uint4 w = v[k];
+      // fp8: the latent part meets fp16 codes in the MMA, so it is fp16 too
+      // (the rope part stays bf16, against the bf16 rope)
+      if (MODE == kSparseFp8 && ch < CPMLA_DV / 8)
+        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                       bf16x2_to_f16x2(w.w));
+      const int kb = ch >> 3, cc = ch & 7;
+      *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
+    }
   }
   fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
   tc_fence_before();
