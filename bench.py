@@ -279,53 +279,108 @@ def main():
     status = cpmla.device_status()
     step_ms = max_over_ranks(attn_avg + merge_avg, world)
 
-    # ---------------- end to end through the public API with host buffers
+    # ---------------- end to end through the public API with host buffers:
+    # every step partitions its batch on the host, copies its inputs and the
+    # partition maps up from pinned host memory and its result back down.
+    # Two buffer sets and three streams pipeline the steps: step i's inputs
+    # go up while step i-1 computes and step i-2's result comes down.
     q_h = prob.q.cpu().pin_memory()
     kv_h = {k: v.cpu().pin_memory() for k, v in kvk.items()}
     sink_h = prob.sink.cpu().pin_memory()
     idx_h = prob.idx.cpu().pin_memory() if prob.idx is not None else None
-    o_h = torch.empty((prob.T, prob.H, 512), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((prob.T, prob.H), dtype=torch.float32).pin_memory()
     cu, qs, dec, kvs = (prob.cu_seqlens.numpy(), prob.q_start_pos.numpy(), prob.is_decode.numpy(),
                         prob.kv_start.numpy())
-    q_d = torch.empty_like(prob.q)
-    kv_d = {k: torch.empty_like(v) for k, v in kvk.items()}
-    sink_d = torch.empty_like(prob.sink)
-    idx_d = torch.empty_like(prob.idx) if prob.idx is not None else None
-    h2d = q_h.numel() * 2 + sum(v.numel() * v.element_size() for v in kv_h.values()) + sink_h.numel() * 4
+    kvs_h = torch.from_numpy(np.ascontiguousarray(kvs, np.int64)).pin_memory()
+    maps = ("rows", "pos", "req", "owner_row")
+    part0 = cpmla.pcp_dualchunk_partition(prob.P, cu, qs, dec)
+    sets = []
+    for _ in range(2):
+        st = {"q": torch.empty_like(prob.q), "kv": {k: torch.empty_like(v) for k, v in kvk.items()},
+              "sink": torch.empty_like(prob.sink),
+              "idx": torch.empty_like(prob.idx) if prob.idx is not None else None,
+              "kv_start": torch.empty(len(kvs), dtype=torch.int64, device=dev),
+              "o": torch.empty((prob.T, prob.H, 512), dtype=torch.bfloat16, device=dev),
+              "lse": torch.empty((prob.T, prob.H), dtype=torch.float32, device=dev),
+              "o_h": torch.empty((prob.T, prob.H, 512), dtype=torch.bfloat16).pin_memory(),
+              "lse_h": torch.empty((prob.T, prob.H), dtype=torch.float32).pin_memory(),
+              "maps_h": {k: torch.empty(len(part0[k]), dtype=torch.int32).pin_memory()
+                         for k in maps},
+              "maps_d": {k: torch.empty(len(part0[k]), dtype=torch.int32, device=dev)
+                         for k in maps},
+              "ev_in": torch.cuda.Event(), "ev_cp": torch.cuda.Event(),
+              "ev_out": torch.cuda.Event()}
+        if not merged:
+            st["o_part"] = torch.empty((plan.n_rows, prob.H, 512), dtype=torch.float32, device=dev)
+            st["lse_part"] = torch.empty((plan.n_rows, prob.H), dtype=torch.float32, device=dev)
+        sets.append(st)
+    s_in, s_cp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    maps_bytes = sum(len(part0[k]) * 4 for k in maps) + kvs_h.numel() * 8
+    h2d = q_h.numel() * 2 + sum(v.numel() * v.element_size() for v in kv_h.values()) + \
+        sink_h.numel() * 4 + maps_bytes
     if idx_h is not None:
         h2d += idx_h.numel() * 4
-    d2h = o_h.numel() * 2 + lse_h.numel() * 4
+    d2h = prob.T * prob.H * (512 * 2 + 4)
 
-    def e2e_step():
-        p = cpmla.PcpPrefill(prob.P, cu, qs, dec, kvs, prob.H, device=dev, topk=prob.topk,
-                             merged=merged)
-        q_d.copy_(q_h, non_blocking=True)
-        for k in kv_d:
-            kv_d[k].copy_(kv_h[k], non_blocking=True)
-        sink_d.copy_(sink_h, non_blocking=True)
-        if idx_d is not None:
-            idx_d.copy_(idx_h, non_blocking=True)
-        p(q_d, softmax_scale=prob.scale, sink=sink_d, idx=idx_d, o_out=o_out, lse_out=lse_out,
-          stream=stream, **kv_d)
-        o_h.copy_(o_out, non_blocking=True)
-        lse_h.copy_(lse_out, non_blocking=True)
-        torch.cuda.synchronize()
-        return p
+    def e2e_step(i):
+        st = sets[i % 2]
+        part = cpmla.pcp_dualchunk_partition(prob.P, cu, qs, dec)  # host
+        st["ev_in"].synchronize()  # the set's last upload has read its pinned maps
+        for k in maps:
+            st["maps_h"][k].numpy()[:] = part[k]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(st["ev_cp"])  # step i-2 has finished reading the set's inputs
+            st["q"].copy_(q_h, non_blocking=True)
+            for k in kv_h:
+                st["kv"][k].copy_(kv_h[k], non_blocking=True)
+            st["sink"].copy_(sink_h, non_blocking=True)
+            if idx_h is not None:
+                st["idx"].copy_(idx_h, non_blocking=True)
+            st["kv_start"].copy_(kvs_h, non_blocking=True)
+            for k in maps:
+                st["maps_d"][k].copy_(st["maps_h"][k], non_blocking=True)
+            st["ev_in"].record(s_in)
+        s_cp.wait_event(st["ev_in"])
+        s_cp.wait_event(st["ev_out"])  # the set's previous result is down
+        m = st["maps_d"]
+        if merged:
+            cpmla.mla_attn_merged(st["q"], st["kv_start"], m["rows"], m["pos"], m["req"],
+                                  m["owner_row"], st["o"], st["lse"], softmax_scale=prob.scale,
+                                  sink=st["sink"], topk_idx=st["idx"], stream=s_cp, **st["kv"])
+        else:
+            if prob.topk:
+                cpmla.mla_partial_attn_sparse(st["q"], st["kv_start"], m["rows"], m["pos"],
+                                              m["req"], st["idx"], st["o_part"], st["lse_part"],
+                                              softmax_scale=prob.scale, stream=s_cp, **st["kv"])
+            else:
+                cpmla.mla_partial_attn_dense(st["q"], st["kv_start"], m["rows"], m["pos"],
+                                             m["req"], st["o_part"], st["lse_part"],
+                                             softmax_scale=prob.scale, stream=s_cp, **st["kv"])
+            cpmla.lse_merge_with_sink(st["o_part"], st["lse_part"], m["owner_row"], st["o"],
+                                      st["lse"], sink=st["sink"], stream=s_cp)
+        st["ev_cp"].record(s_cp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(st["ev_cp"])
+            st["o_h"].copy_(st["o"], non_blocking=True)
+            st["lse_h"].copy_(st["lse"], non_blocking=True)
+            st["ev_out"].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
-    # the partition maps' uploads are part of the step too
-    maps_bytes = sum(getattr(e2e_step(), k).numel() * 4 for k in ("rows", "pos", "req", "owner_row"))
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        flush.fill_(2.0)
-        e2e_step()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world)
+    # the result of the last step, checked against the timed path's output
+    # (the first and last 128 tokens)
+    last = sets[(args.e2e_steps - 1) % 2]
+    for sl in (slice(0, 128), slice(max(0, prob.T - 128), prob.T)):
+        assert torch.equal(last["o_h"][sl].view(torch.int16), o_out[sl].cpu().view(torch.int16))
 
     # ---------------- roofline (attention kernel) and merge bandwidth
     pk = peaks()
@@ -364,8 +419,11 @@ def main():
                            "unit": "GB/s", "frac": round(merge_gbs / pk["hbm"], 4),
                            "bytes": merge_bytes, "kernel": "lse_merge_kernel (two-launch path)"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d + maps_bytes,
-                "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "how": "per step: host partition, inputs + maps up from pinned memory, one "
+                       "path call, O + LSE down; steps pipelined over two buffer sets and "
+                       "three streams"},
         "gpu_launches": (1 if merged else 2) * args.steps,
         "clocks": clk.summary(),
         "device_status": status,

@@ -266,8 +266,11 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         }
     }
     c.n_tiles = (last + kTileKeys) / kTileKeys;
-    // merged: the global token this CTA writes, if its row owns it (a
-    // decode row is computed once per shard, owned by one)
+    fence_mbar_init();
+  }
+  if (tid == 32) {
+    // merged: the global token this CTA writes, if its row owns it (a decode
+    // row is computed once per shard, owned by one); beside thread 0's loads
     c.gtok = -1;
     if (MERGED && row < a.n_rows) {
       const int g = a.rows[row];
@@ -276,7 +279,6 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
       else if (a.owner_row[g] == row)
         c.gtok = g;
     }
-    fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
   if (tid < R) {
