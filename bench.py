@@ -33,9 +33,9 @@ import torch  # noqa: E402
 
 METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 roofline"
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
-# capture summarised in profiles/ (per workload; None = not captured for the
-# current kernel).  Must be reset to None whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {}
+# capture summarised in profiles/ (per workload and path; None = not captured
+# for the current kernel).  Must be reset whenever that kernel changes.
+NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
@@ -412,7 +412,7 @@ def main():
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16"], 4),
-                     "traffic": NCU_TRAFFIC_BYTES.get(args.workload),
+                     "traffic": NCU_TRAFFIC_BYTES.get((args.workload, args.path)),
                      "kernel": "mla_sparse_kernel" if prob.topk else "mla_dense_kernel",
                      "peak_source": pk["source"] + " burst bf16"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm"],
