@@ -326,3 +326,88 @@ void oracle_merge(int T, int H, const double *o_part, const double *lse_part,
     }
   }
 }
+
+/* --------------------------------------------------------- cache insertion */
+/*
+ * "[Core] Add MRV2 virtual-batch PCP for MLA", Summary (sparse MLA cache
+ * insertion) and "DualChunkSwap partitioning" (the all-gathered latent KV is
+ * what the cache insertion writes); the "fp8_ds_mla" KV-cache dtype of
+ * "[Feature][PCP] Add DeepSeek-V4.1-Flash support".  The pages fix neither
+ * the fp8 layout nor the quantisation rule.  Readings (R13):
+ *   token t with slot s >= 0 goes to cache row s; s = -1 skips the token;
+ *   bf16 cache: the 576 values copied;
+ *   fp8 cache (R8 layout): per 128-channel latent group, amax = max |x|,
+ *   scale = amax / 448 in binary32 (1 when amax == 0), code = E4M3(x / scale)
+ *   with the quotient in binary32 and E4M3 rounding to nearest, ties to even,
+ *   saturating at +-448; the rope copied as bf16.
+ * The codes are integers decided by binary32 arithmetic, so the oracle takes
+ * those decisions in binary32 -- the precision the kernel takes them in.
+ */
+
+/* Round-half-to-even of a non-negative double to an integer value. */
+static double orc_round_half_even(double q) {
+  double fl = floor(q), d = q - fl;
+  if (d > 0.5) return fl + 1.0;
+  if (d < 0.5) return fl;
+  return fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;
+}
+
+/* binary32 -> OCP E4M3 byte (R8 format: 3 fraction bits, exponent bias 7,
+ * normal exponents -6..8, subnormals m * 2^-9): round to nearest, ties to
+ * even; every finite value at or above 448 in magnitude (and infinity)
+ * saturates to +-448; NaN gives 0x7F. */
+uint8_t oracle_e4m3_encode(float f) {
+  if (isnan(f)) return 0x7F;
+  const uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  const double a = fabs((double)f);
+  if (a >= 448.0) return sign | 0x7E; /* 448 is the largest finite value */
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2);        /* a = frac * 2^e2, frac in [0.5, 1) */
+  int ex = e2 - 1;      /* floor(log2 a) */
+  if (ex < -6) ex = -6; /* below 2^-6 the subnormal step 2^-9 */
+  const double quantum = ldexp(1.0, ex - 3);
+  const double v = orc_round_half_even(a / quantum) * quantum; /* <= 448 */
+  if (v == 0.0) return sign;
+  int ev2;
+  frexp(v, &ev2);
+  const int ev = ev2 - 1;
+  if (ev < -6) return sign | (uint8_t)(v / ldexp(1.0, -9)); /* subnormal m */
+  const int m = (int)((v / ldexp(1.0, ev) - 1.0) * 8.0);
+  return sign | (uint8_t)(((ev + 7) << 3) | m);
+}
+
+/* Insert n tokens' latent KV (bf16 [n, 576]) into the cache rows slot[t]
+ * (R13).  fmt 0: cache_bf16 [s_cache, 576]; fmt 1: cache_fp8 [s_cache, 512],
+ * cache_scale [s_cache, 4], cache_rope [s_cache, 64].  Returns -1 if a slot
+ * lies outside [-1, s_cache). */
+int oracle_kv_insert(int n, const uint16_t *kv, const int64_t *slot, int fmt, long long s_cache,
+                     uint16_t *cache_bf16, uint8_t *cache_fp8, float *cache_scale,
+                     uint16_t *cache_rope) {
+  for (int t = 0; t < n; ++t)
+    if (slot[t] < -1 || slot[t] >= s_cache) return -1;
+  for (int t = 0; t < n; ++t) {
+    const long long s = slot[t];
+    if (s < 0) continue;
+    const uint16_t *x = kv + (long long)t * ORC_DQK;
+    if (fmt == 0) {
+      memcpy(cache_bf16 + s * ORC_DQK, x, ORC_DQK * sizeof(uint16_t));
+      continue;
+    }
+    for (int g = 0; g < ORC_DV / ORC_GROUP; ++g) {
+      float amax = 0.0f;
+      for (int d = 0; d < ORC_GROUP; ++d) {
+        const float v = fabsf((float)oracle_bf16_to_double(x[g * ORC_GROUP + d]));
+        if (v > amax) amax = v;
+      }
+      const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      cache_scale[s * 4 + g] = scale;
+      for (int d = 0; d < ORC_GROUP; ++d) {
+        const float v = (float)oracle_bf16_to_double(x[g * ORC_GROUP + d]);
+        cache_fp8[s * ORC_DV + g * ORC_GROUP + d] = oracle_e4m3_encode(v / scale);
+      }
+    }
+    memcpy(cache_rope + s * ORC_DROPE, x + ORC_DV, ORC_DROPE * sizeof(uint16_t));
+  }
+  return 0;
+}

@@ -59,6 +59,11 @@ def _load():
                  _P, ctypes.c_int, _P, _P, ctypes.c_double, _P, _P, _P])
             lib.oracle_merge.restype = None
             lib.oracle_merge.argtypes = [ctypes.c_int, ctypes.c_int] + [_P] * 7
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            lib.oracle_kv_insert.restype = ctypes.c_int
+            lib.oracle_kv_insert.argtypes = ([ctypes.c_int, _P, _P, ctypes.c_int,
+                                              ctypes.c_longlong] + [_P] * 4)
             _lib = lib
     return _lib
 
@@ -189,3 +194,37 @@ def pcp_attention(P, cu_seqlens, q_start_pos, is_decode, q_bits, kv_start_req, *
     T = len(part["owner_row"])
     off = np.arange(T + 1, dtype=np.int32)
     return merge(o_p, l_p, off, part["owner_row"], sink=sink)
+
+
+def e4m3_encode(values: np.ndarray) -> np.ndarray:
+    """binary32 -> OCP E4M3 bytes, round to nearest even, saturating to
+    +-448 (oracle encoder, from the format definition)."""
+    lib = _load()
+    flat = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in flat],
+                    dtype=np.uint8).reshape(np.shape(values))
+
+
+def kv_insert(kv_bits, slot, *, fmt, s_cache, cache=None):
+    """Insert tokens' latent KV (bf16 bits [n, 576]) into cache rows slot[t]
+    (-1 skips), bf16 (fmt 0) or fp8 (fmt 1; per-128-channel amax/448 scales,
+    E4M3 codes), as "[Core] Add MRV2 virtual-batch PCP for MLA" inserts the
+    all-gathered latent KV into the cache; the quantisation rule is the
+    reading R13 of the repository's design notes.  `cache` (dict of numpy
+    arrays) is updated in place and returned; fresh zero arrays if None."""
+    lib = _load()
+    kv = _c(kv_bits, np.uint16)
+    n = kv.shape[0]
+    sl = _c(slot, np.int64)
+    if cache is None:
+        cache = (dict(kv=np.zeros((s_cache, DQK), np.uint16)) if fmt == 0 else
+                 dict(kv_fp8=np.zeros((s_cache, DV), np.uint8),
+                      kv_scale=np.zeros((s_cache, DV // GROUP), np.float32),
+                      kv_rope=np.zeros((s_cache, DROPE), np.uint16)))
+    rc = lib.oracle_kv_insert(n, _ptr(kv), _ptr(sl), fmt, s_cache, _ptr(cache.get("kv")),
+                              _ptr(cache.get("kv_fp8")), _ptr(cache.get("kv_scale")),
+                              _ptr(cache.get("kv_rope")))
+    if rc != 0:
+        raise ValueError("oracle_kv_insert: a slot lies outside [-1, s_cache)")
+    return cache
+
