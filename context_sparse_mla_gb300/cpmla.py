@@ -43,6 +43,7 @@ _SIGS = {
                                    _P, _P, _F, _P, _I, _P, _P, _P, _P]),
     "mla_attn_sparse_merged": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I,
                                     _P, _P, _P, _I, _F, _P, _I, _P, _P, _P, _P]),
+    "mla_kv_cache_insert": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P, _P, _I64, _P]),
 }
 
 _lock = threading.Lock()
@@ -191,6 +192,27 @@ def mla_attn_merged(q, kv_start, rows, pos, req, owner_row, o_out, lse_out, *, s
     else:
         _dev(topk_idx, torch.int32, "topk_idx")
         _check(lib().mla_attn_sparse_merged(*common, _ptr(topk_idx), topk_idx.shape[1], *tail))
+
+
+def mla_kv_cache_insert(kv, slot_mapping, *, cache=None, cache_fp8=None, cache_scale=None,
+                        cache_rope=None, stream=None):
+    """Write each token's latent KV row (kv [n, 576] bf16) to its cache row
+    slot_mapping[t] (int64, -1 skips): a bf16 cache [S, 576], or the fp8 one
+    (cache_fp8 [S, 512] E4M3, cache_scale [S, 4] fp32, cache_rope [S, 64])."""
+    fmt = CPMLA_KV_BF16 if cache is not None else CPMLA_KV_FP8_E4M3_G128
+    if fmt == CPMLA_KV_BF16:
+        _dev(cache, torch.bfloat16, "cache")
+        s_cache = cache.shape[0]
+    else:
+        _dev(cache_fp8, torch.uint8, "cache_fp8")
+        _dev(cache_scale, torch.float32, "cache_scale")
+        _dev(cache_rope, torch.bfloat16, "cache_rope")
+        s_cache = cache_fp8.shape[0]
+    _dev(kv, torch.bfloat16, "kv")
+    _check(lib().mla_kv_cache_insert(
+        _ptr(kv), kv.stride(0), kv.shape[0], _ptr(_dev(slot_mapping, torch.int64, "slot_mapping")),
+        fmt, _ptr(cache), _ptr(cache_fp8), _ptr(cache_scale), _ptr(cache_rope), s_cache,
+        _stream(stream)))
 
 
 def lse_merge_with_sink(o_part, lse_part, contrib_rows, o_out, lse_out, *, contrib_off=None,

@@ -227,6 +227,47 @@ int mla_attn_sparse_merged(const void *q, int64_t q_token_stride, int H, int kv_
                            float *lse_out, void *stream);
 
 /* --------------------------------------------------------------------------
+ * 2c. Latent KV-cache insertion (device)
+ *
+ * "[Core] Add MRV2 virtual-batch PCP for MLA", Summary (sparse MLA cache
+ * insertion) and "DualChunkSwap partitioning" (every rank holds the
+ * all-gathered latent KV it inserts into the cache); the fp8_ds_mla cache
+ * dtype of "[Feature][PCP] Add DeepSeek-V4.1-Flash support".  Token t's row
+ * kv[t] (bf16, 512 latent + 64 rope) goes to cache row slot_mapping[t]; a
+ * slot of -1 skips the token.  The pages give no quantisation rule; this is
+ * the library's own:
+ *   CPMLA_KV_BF16          cache[s, :] = kv[t, :]
+ *   CPMLA_KV_FP8_E4M3_G128 per 128-channel latent group g:
+ *                          amax = max |kv[t, 128g .. 128g+127]|,
+ *                          scale = amax / 448 in binary32 (1 if amax == 0),
+ *                          cache_fp8[s, c] = E4M3(kv[t, c] / scale), the
+ *                          quotient in binary32, round to nearest even,
+ *                          saturating at +-448 (NaN stays NaN);
+ *                          cache_scale[s, g] = scale; cache_rope[s, :] =
+ *                          kv[t, 512:576]
+ * so that the fp8 attention's value kv_fp8 * kv_scale is within half an E4M3
+ * step of the bf16 input.
+ *
+ * Arguments (device unless noted):
+ *   kv             bf16 [n, 576], token t at kv + t * kv_token_stride
+ *                  (elements, host, >= 576, multiple of 8); 16-byte aligned
+ *   n              tokens (host); 0 is a no-op
+ *   slot_mapping   int64 [n]: cache row of each token, or -1
+ *   kv_format      CPMLA_KV_* (host)
+ *   cache          bf16 [s_cache, 576] (bf16 format), 16-byte aligned
+ *   cache_fp8      uint8 [s_cache, 512], cache_scale fp32 [s_cache, 4],
+ *                  cache_rope bf16 [s_cache, 64] (fp8 format); the first and
+ *                  last 16-byte aligned
+ *   s_cache        cache rows (host)
+ * Slots must be distinct (two tokens writing one row race).  A slot outside
+ * [-1, s_cache) is skipped and recorded as CPMLA_ERR_INDEX in the status word.
+ * Errors: CPMLA_ERR_ARG, CPMLA_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+int mla_kv_cache_insert(const void *kv, int64_t kv_token_stride, int n,
+                        const int64_t *slot_mapping, int kv_format, void *cache, void *cache_fp8,
+                        float *cache_scale, void *cache_rope, int64_t s_cache, void *stream);
+
+/* --------------------------------------------------------------------------
  * 3. Global LSE merge + attention sink once + restore to global order (device)
  *
  * "[DeepSeekV4][PCP] ...", "Implementation summary" (merge LSE/output

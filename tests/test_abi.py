@@ -36,7 +36,8 @@ def _declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert {"pcp_dualchunk_partition", "mla_partial_attn_dense", "mla_partial_attn_sparse",
-            "lse_merge_with_sink", "mla_attn_dense_merged", "mla_attn_sparse_merged"} <= set(names)
+            "lse_merge_with_sink", "mla_attn_dense_merged", "mla_attn_sparse_merged",
+            "mla_kv_cache_insert"} <= set(names)
     h = ctypes.CDLL(cpmla.LIB_PATH)
     for n in names:
         assert hasattr(h, n), n
@@ -127,6 +128,17 @@ def test_merged_attention_argument_checks(lib):
     assert b"o_out" in lib.cpmla_last_error()
     assert lib.mla_attn_sparse_merged(*base, 1, None, None, None, 8, 0.07, None, -1, None, None,
                                       None, None) == cpmla.CPMLA_ERR_ARG
+
+
+def test_kv_cache_insert_argument_checks(lib):
+    f = lib.mla_kv_cache_insert
+    assert f(None, 576, 0, None, 0, None, None, None, None, 16, None) == cpmla.CPMLA_OK
+    assert f(None, 576, 4, None, 0, None, None, None, None, 16, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 576, 4, None, 5, None, None, None, None, 16, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 500, 4, None, 0, None, None, None, None, 16, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 576, 4, None, 0, None, None, None, None, 0, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 576, -1, None, 0, None, None, None, None, 16, None) == cpmla.CPMLA_ERR_ARG
+    assert b"mla_kv_cache_insert" in lib.cpmla_last_error()
 
 
 def test_merge_argument_checks(lib):

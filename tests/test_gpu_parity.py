@@ -223,6 +223,44 @@ def test_merged_epilogue_full_size_dense_sampled():
     pu.compare(o[ti], lse[ti], ro, rl)
 
 
+# ------------------------------------------------------------- cache insertion
+def _insert_case(n, s_cache, seed, fmt):
+    g = torch.Generator().manual_seed(seed)
+    kv = (torch.randn((n, 576), generator=g) * torch.exp(torch.randn((n, 1), generator=g)))
+    kv = kv.to(torch.bfloat16)
+    kv[min(3, n - 1), 128:256] = 0  # an all-zero group
+    slot = torch.randperm(s_cache, generator=g)[:n].to(torch.int64)
+    slot[:: max(1, n // 7)] = -1  # skipped tokens
+    bits = kv.view(torch.int16).numpy().view(np.uint16)
+    want = orc.kv_insert(bits, slot.numpy(), fmt=fmt, s_cache=s_cache)
+    if fmt == 0:
+        cache = torch.zeros((s_cache, 576), dtype=torch.bfloat16, device="cuda")
+        cpmla.mla_kv_cache_insert(kv.cuda(), slot.cuda(), cache=cache)
+        got = dict(kv=cache.cpu().view(torch.int16).numpy().view(np.uint16))
+    else:
+        c8 = torch.zeros((s_cache, 512), dtype=torch.uint8, device="cuda")
+        cs = torch.zeros((s_cache, 4), dtype=torch.float32, device="cuda")
+        cr = torch.zeros((s_cache, 64), dtype=torch.bfloat16, device="cuda")
+        cpmla.mla_kv_cache_insert(kv.cuda(), slot.cuda(), cache_fp8=c8, cache_scale=cs,
+                                  cache_rope=cr)
+        got = dict(kv_fp8=c8.cpu().numpy(), kv_scale=cs.cpu().numpy(),
+                   kv_rope=cr.cpu().view(torch.int16).numpy().view(np.uint16))
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    for k in want:  # bytes and binary32 scales: bit-exact
+        assert np.array_equal(got[k].view(np.uint8), want[k].view(np.uint8)), k
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_kv_cache_insert_bit_exact(fmt):
+    _insert_case(3001, 4000, 30 + fmt, fmt)
+
+
+def test_kv_cache_insert_fp8_full_size():
+    """The fp8 cache of the 131072-token sparse workload, every token inserted."""
+    _insert_case(131072, 131072 + 5, 32, 1)
+
+
 def test_merge_kernel_against_oracle_merge():
     rng = np.random.default_rng(17)
     n_part, H, T = 300, 6, 120
