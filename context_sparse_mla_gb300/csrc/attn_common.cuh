@@ -138,20 +138,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&t);
 }
 
-// Global KV row of entry e of shard row `row`'s top-k list, or -1 when the
-// entry is empty, outside the row's causal prefix or KV, or outside its
-// optional [kv_lo, kv_hi] restriction.
-__device__ __forceinline__ int64_t sparse_key_src(const AttnArgs &a, int row, int e) {
-  if (e >= a.k) return -1;
-  const int p = a.topk[(int64_t)a.rows[row] * a.k + e];
-  const int tpos = a.pos[row];
-  if (p < 0 || p > tpos) return -1;
-  if (a.kv_lo && p < a.kv_lo[row]) return -1;
-  if (a.kv_hi && p > a.kv_hi[row]) return -1;
-  const int64_t src = a.kv_start[a.req[row]] + p;
-  return src < a.s_kv ? src : -1;
-}
-
 // Elected bounded wait whose result every thread of a named-barrier group
 // sees (so no thread skips a barrier the others enter).
 __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, int t, int bar_id,

@@ -1,5 +1,5 @@
 // cpmla_internal.cuh -- shared plumbing of libcpmla.so: error reporting and the
-// inline-PTX wrappers (mbarrier, TMA, cp.async, tcgen05/TMEM) used by the
+// inline-PTX wrappers (mbarrier, TMA, bulk copies, tcgen05/TMEM) used by the
 // sm_103a kernels.  Nothing here is part of the public ABI.
 #pragma once
 
@@ -142,21 +142,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
 
-// --- cp.async (16 B, zero-fill when src_bytes == 0)
-__device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-// Arrive on an mbarrier once every cp.async issued so far by this thread has
-// landed (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
 // --- bulk copy shared -> global (TMA, no tensor map): both addresses 16-byte
 // aligned, bytes a multiple of 16
 __device__ __forceinline__ void bulk_store_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
@@ -170,10 +155,6 @@ __device__ __forceinline__ void bulk_commit() {
 // until the committed bulk stores have read their shared-memory source
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // --- tcgen05: TMEM allocation (whole warp)
