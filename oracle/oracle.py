@@ -228,3 +228,29 @@ def kv_insert(kv_bits, slot, *, fmt, s_cache, cache=None):
         raise ValueError("oracle_kv_insert: a slot lies outside [-1, s_cache)")
     return cache
 
+
+def topk_select(logits, row_len, k):
+    """Top-k selection of an indexer's logits (the step "[Feat][NVIDIA]
+    DeepSeek-V4.1: Prefill support CP with multistream forward prepare (4/N)"
+    runs after mqa_logits, its topk_v2): for row i, among columns
+    0 .. row_len[i]-1, the k largest values -- ties to the smaller column --
+    returned as column indices in ascending order, -1 padded; a row with at
+    most k candidates returns all of them.  Values are ordered by the IEEE
+    total order of non-NaN binary32 (-0 below +0), the reading R14 of the
+    repository's design notes.  logits: float32 [n_rows, >= max(row_len)].
+    Returns int32 [n_rows, k]."""
+    x = np.asarray(logits, dtype=np.float32)
+    lens = np.asarray(row_len, dtype=np.int64)
+    out = np.full((x.shape[0], k), -1, dtype=np.int32)
+    for i in range(x.shape[0]):
+        n = int(lens[i])
+        if n <= k:
+            out[i, :n] = np.arange(n, dtype=np.int32)
+            continue
+        bits = x[i, :n].view(np.uint32).astype(np.int64)
+        # an order-preserving integer image of the floats (total order)
+        key = np.where(bits >> 31 == 1, 0xFFFFFFFF - bits, bits + 0x80000000)
+        order = np.lexsort((np.arange(n), -key))  # value descending, column ascending
+        out[i] = np.sort(order[:k]).astype(np.int32)
+    return out
+
