@@ -35,7 +35,8 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472}
+NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
+                     ("topk_s8k_k2048", "topk"): 126_343_936 + 8_413_952}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
@@ -259,6 +260,140 @@ def run_kv_insert(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+TOPK_WORKLOADS = {"topk_s32k_k2048": 32768, "topk_s8k_k2048": 8192}
+
+
+def run_topk(args, world, rank, local):
+    """The indexer's top-k selection over one causal request: logits fp32
+    [S, S] (row t holds the scores of query t against keys 0..t), k = 2048.
+    Reports GB/s of algorithmic bytes (the causal logits of rows longer than
+    k read once, the row lengths read, the index lists written) against the
+    measured HBM copy bandwidth.  --impl reference times the oracle on rows."""
+    S, k = TOPK_WORKLOADS[args.workload], 2048
+    rl_h = torch.arange(1, S + 1, dtype=torch.int32)
+    n = rl_h.to(torch.int64)
+    bytes_step = int(4 * n[n > k].sum()) + 4 * S + 4 * S * k
+    cfg = {"workload": args.workload, "rows": S, "k": k, "logits": "fp32 [S, S], causal rows",
+           "l2": "flushed between steps (512 MiB write); the logits read exceed L2",
+           "parallelism": "replicas (one full workload per GPU)" if world > 1 else "single GPU"}
+    metric = "indexer top-k selection GB/s"
+    data = "synthetic (seeded N(0,1) fp32 logits standing in for indexer scores)"
+    if args.impl == "reference":
+        if rank == 0:
+            from oracle import oracle as orc
+            rows = np.arange(S - 64, S)  # the longest rows
+            x = synth_logits(args.workload, rows, args.seed)
+            vals = []
+            for i in range(args.warmup + args.steps):
+                t0 = time.perf_counter()
+                orc.topk_select(x, rl_h[rows].numpy(), k)
+                if i >= args.warmup:
+                    vals.append(rows_bytes(rl_h[rows], k) / (time.perf_counter() - t0) / 1e9)
+            v = statistics.median(vals)
+            print(json.dumps({"impl": "reference", "metric": metric, "value": round(v, 4),
+                              "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+                              "warmup": args.warmup, "higher_is_better": True, "config": cfg,
+                              "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(v, 4),
+                                               "sample": "the 64 longest rows per step"},
+                              "e2e": {"value": round(v, 4), "unit": "GB/s",
+                                      "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+                  flush=True)
+        return
+    from context_sparse_mla_gb300 import build as cbuild
+    from context_sparse_mla_gb300 import cpmla, synth
+    cbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = synth.indexer_logits(S, S, seed=args.seed, device=dev)
+    rl = rl_h.to(dev)
+    out = torch.empty((S, k), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cpmla.mla_topk_select(x, rl, k, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, world)
+    # last step's lists on a few rows against the oracle (outside the timing)
+    check_rows = torch.tensor([k, S // 2, S - 1], device=dev)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import oracle as orc
+        want = orc.topk_select(x[check_rows].cpu().numpy(), rl_h[check_rows.cpu()].numpy(), k)
+        assert np.array_equal(out[check_rows].cpu().numpy(), want), "top-k check failed"
+        rows = np.arange(S - 256, S)
+        xs = x[torch.as_tensor(rows, device=dev)].cpu().numpy()
+        t0 = time.perf_counter()
+        orc.topk_select(xs, rl_h[rows].numpy(), k)
+        dt = time.perf_counter() - t0
+        v = rows_bytes(rl_h[rows], k) / dt / 1e9
+        cpu = {"kind": "oracle", "cores": 1, "value": round(v, 4), "unit": "GB/s",
+               "sample": "the 256 longest rows (%.1f s)" % dt}
+    # end to end: the logits and row lengths up from pinned memory, the lists down
+    x_h = torch.empty((S, S), dtype=torch.float32).pin_memory()
+    x_h.copy_(x)
+    rl_p = rl_h.pin_memory()
+    out_h = torch.empty((S, k), dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        x.copy_(x_h, non_blocking=True)
+        rl.copy_(rl_p, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.e2e_steps, world)
+    pk = peaks()
+    gbs = world * bytes_step / (ms * 1e-3) / 1e9
+    res = {"metric": metric, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": data, "config": cfg,
+           "roofline": {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": pk["hbm"],
+                        "unit": "GB/s", "frac": round(gbs / world / pk["hbm"], 4),
+                        "traffic": NCU_TRAFFIC_BYTES.get((args.workload, "topk")),
+                        "kernel": "topk_select_kernel",
+                        "peak_source": pk["source"] + " HBM copy"},
+           "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": 4 * S * S + 4 * S,
+                   "d2h_bytes_per_step": 4 * S * k},
+           "gpu_launches": args.steps, "clocks": clk.summary(),
+           "device_status": cpmla.device_status(), "cpu_baseline": cpu}
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def rows_bytes(row_len, k):
+    """Algorithmic bytes of the selection of these rows (as in run_topk)."""
+    n = row_len.to(torch.int64)
+    return int(4 * n[n > k].sum()) + 4 * len(n) + 4 * len(n) * k
+
+
+def synth_logits(workload, rows, seed):
+    """Rows of the workload's logits, drawn as the GPU arm draws them (on the
+    GPU when there is one, else the same generator on the host)."""
+    from context_sparse_mla_gb300 import synth
+    S = TOPK_WORKLOADS[workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = synth.indexer_logits(S, S, seed=seed, device=dev)
+    return x[torch.as_tensor(rows, device=dev)].cpu().numpy()
+
+
 def workload_config(name, prob, world):
     return {"workload": name, "tokens": prob.T, "heads": prob.H, "pcp": prob.P,
             "topk": prob.topk, "kv_format": prob.kv_format,
@@ -325,6 +460,9 @@ def main():
 
     if args.workload == KV_INSERT_WORKLOAD:
         run_kv_insert(args, world, rank, local)
+        return
+    if args.workload in TOPK_WORKLOADS:
+        run_topk(args, world, rank, local)
         return
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -44,6 +44,7 @@ _SIGS = {
     "mla_attn_sparse_merged": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I,
                                     _P, _P, _P, _I, _F, _P, _I, _P, _P, _P, _P]),
     "mla_kv_cache_insert": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P, _P, _I64, _P]),
+    "mla_topk_select": (_I, [_P, _I64, _I, _P, _I, _I, _P, _P]),
 }
 
 _lock = threading.Lock()
@@ -213,6 +214,25 @@ def mla_kv_cache_insert(kv, slot_mapping, *, cache=None, cache_fp8=None, cache_s
         _ptr(kv), kv.stride(0), kv.shape[0], _ptr(_dev(slot_mapping, torch.int64, "slot_mapping")),
         fmt, _ptr(cache), _ptr(cache_fp8), _ptr(cache_scale), _ptr(cache_rope), s_cache,
         _stream(stream)))
+
+
+def mla_topk_select(logits, row_len, k, *, max_row_len=None, out=None, stream=None):
+    """Per row i, the k columns of the largest logits[i, :row_len[i]] (IEEE
+    total order, ties to the smaller column) in ascending order, -1 padded:
+    logits fp32 [n_rows, L] (L a multiple of 4), row_len int32 [n_rows].
+    Returns int32 [n_rows, k] (``out`` if given)."""
+    _dev(logits, torch.float32, "logits")
+    _dev(row_len, torch.int32, "row_len")
+    n_rows, width = logits.shape
+    if out is None:
+        out = torch.empty((n_rows, k), dtype=torch.int32, device=logits.device)
+    _dev(out, torch.int32, "out")
+    if out.shape != (n_rows, k):
+        raise ValueError("out must be [%d, %d]" % (n_rows, k))
+    _check(lib().mla_topk_select(
+        _ptr(logits), width, n_rows, _ptr(row_len), width if max_row_len is None else max_row_len,
+        k, _ptr(out), _stream(stream)))
+    return out
 
 
 def lse_merge_with_sink(o_part, lse_part, contrib_rows, o_out, lse_out, *, contrib_off=None,

@@ -1,0 +1,524 @@
+// topk.cu -- the indexer's top-k selection: per query row, the k largest of
+// its logits over the request's causal prefix, as request-local positions in
+// ascending order (-1 padded), the index list the sparse attention reads.
+//
+// "[Feat][NVIDIA] DeepSeek-V4.1: Prefill support CP with multistream forward
+// prepare (4/N)" (the indexer: mqa_logits scores, topk_v2 selects); the
+// selection rule: values ordered by the IEEE total order of non-NaN binary32
+// (-0 below +0), ties to the smaller column, a row with at most k candidates
+// returning all of them.
+//
+// HBM-bound: a row of n > k logits is read once (4n bytes) and 4k bytes of
+// indices are written.  Persistent CTAs take rows in turn, longest first; a
+// bulk L2 prefetch of a CTA's next row is issued as soon as its current row
+// has been filtered, so HBM streams while the selection runs on chip.  Per
+// row:
+//   1. sample: 256 groups of 8 consecutive logits spread over the row; the
+//      threshold c is the sample's r-th largest, r chosen so that about
+//      k + 3 standard deviations of the row are expected at or above it;
+//      rows of at most C logits skip this (c = -inf).
+//   2. filter: one coalesced pass keeps every logit >= c, with its column,
+//      as a candidate in shared memory (warp-aggregated appends).
+//   3. exact selection over the candidates when there are between k and C of
+//      them (then every logit below c ranks below the k-th largest): a radix
+//      select over the candidates' key range gives the k-th largest key tau,
+//      how many keys exceed it and how many equal it.
+//   4. a bitmap over the row's columns marks the keys above tau and, cut in
+//      column order, the ties; a scan of its words writes the k columns in
+//      ascending order.
+// When the sample's threshold fails (fewer than k or more than C logits at or
+// above it), steps 3-4 run over the row in global memory instead: slower,
+// the same result.
+#include <algorithm>
+#include <cmath>
+
+#include "cpmla_internal.cuh"
+
+namespace cpmla {
+namespace {
+
+constexpr int kTkThreads = 256;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kSample = 2048;     // sampled logits: one group of 8 per thread
+constexpr int kFilterUnroll = 4;  // float4 loads per thread in flight in the filter pass
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kRankDirect = 64;   // a bin this small is finished by direct ranking
+constexpr int kDigitBits = 8;     // radix digit: 256 bins, one per thread in the scan
+constexpr int kBins = 1 << kDigitBits;
+constexpr int kBinsPerThread = kBins / kTkThreads;
+constexpr int kPrefetchChunk = 32768;
+
+static_assert(kSample == 8 * kTkThreads, "one sample group of 8 logits per thread");
+static_assert(kBinsPerThread * kTkThreads == kBins, "whole bins per thread");
+
+// order-preserving image of a binary32 value: unsigned compare of keys is the
+// IEEE total order (-0 below +0)
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(v);
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+// Starts streaming a row's logits into L2 (in-bounds: the row's allocation
+// holds its length rounded up to a multiple of 4 floats).
+__device__ __forceinline__ void prefetch_row_l2(const float *x, int n) {
+  const int64_t bytes = (((int64_t)n * 4) + 15) & ~(int64_t)15;
+  for (int64_t off = 0; off < bytes; off += kPrefetchChunk) {
+    const int64_t left = bytes - off;
+    const uint32_t sz = (uint32_t)(left < kPrefetchChunk ? left : kPrefetchChunk);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                     reinterpret_cast<const char *>(x) + off),
+                 "r"(sz)
+                 : "memory");
+  }
+}
+
+struct TkScratch {
+  int hist[kBins];
+  int wsum[kTkWarps];
+  uint32_t rlo[kTkWarps], rhi[kTkWarps];
+  int cnt;       // candidates appended by the filter pass
+  int bin, above, in_bin;  // the bin holding the wanted rank, counts above and in it
+  int cut;       // last tie column kept
+  int total;     // columns marked in the bitmap
+  int n_small;   // keys gathered for direct ranking
+  uint32_t tau;  // direct ranking result: key, elements above and equal
+  int gt, eq;
+  uint32_t small[kRankDirect];
+};
+
+struct Selection {
+  uint32_t tau;  // key of the kth-largest element
+  int n_gt;      // elements with key > tau (< kth)
+  int n_eq;      // elements with key == tau (n_gt + n_eq >= kth)
+};
+
+// Inclusive scan of one int per thread over the block.
+__device__ __forceinline__ int block_incl_scan(int v, TkScratch &sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) sc.wsum[warp] = v;
+  __syncthreads();
+  int add = 0;
+  for (int w = 0; w < warp; ++w) add += sc.wsum[w];
+  __syncthreads();
+  return v + add;
+}
+
+// Smallest and largest of each thread's (lo, hi) over the block.
+__device__ __forceinline__ void block_minmax(uint32_t &lo, uint32_t &hi, TkScratch &sc) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    sc.rlo[warp] = lo;
+    sc.rhi[warp] = hi;
+  }
+  __syncthreads();
+  lo = sc.rlo[0];
+  hi = sc.rhi[0];
+  for (int w = 1; w < kTkWarps; ++w) {
+    lo = min(lo, sc.rlo[w]);
+    hi = max(hi, sc.rhi[w]);
+  }
+  __syncthreads();
+}
+
+// Radix select of the kth-largest key (1 <= kth <= count) among
+// key_at(0 .. count-1), whose smallest and largest keys are kmin and kmax.
+// Digits of kDigitBits are taken from the top of the keys' range
+// (key - kmin), so the first histogram already spreads over it; once the bin
+// holding the wanted rank has at most kRankDirect keys they are gathered and
+// ranked against each other.  Called by every thread; ends with a barrier.
+template <class KeyAt>
+__device__ Selection block_select(const KeyAt &key_at, int count, int kth, uint32_t kmin,
+                                  uint32_t kmax, TkScratch &sc) {
+  const int tid = threadIdx.x;
+  if (kmin == kmax) return {kmax, 0, count};
+
+  int hib = 32 - __clz((int)(kmax - kmin));  // bits hib.. of (key - kmin) are zero
+  uint32_t fixed = 0;                          // (key - kmin) >> hib of the wanted element
+  int krem = kth, n_gt = 0, in_bin = count;
+  while (in_bin > kRankDirect) {
+    const int lob = max(hib - kDigitBits, 0), nb = 1 << (hib - lob);
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) sc.hist[tid + j * kTkThreads] = 0;
+    __syncthreads();
+    for (int i = tid; i < count; i += kTkThreads) {
+      const uint32_t u = key_at(i) - kmin;
+      const uint32_t high = hib >= 32 ? 0u : (u >> hib);
+      if (high == fixed) atomicAdd(&sc.hist[(u >> lob) & (uint32_t)(nb - 1)], 1);
+    }
+    __syncthreads();
+    // bins from the top, kBinsPerThread consecutive ones per thread
+    int h[kBinsPerThread], sum = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      const int bin = nb - 1 - kBinsPerThread * tid - j;
+      h[j] = bin >= 0 ? sc.hist[bin] : 0;
+      sum += h[j];
+    }
+    const int incl = block_incl_scan(sum, sc);
+    if (incl - sum < krem && krem <= incl) {
+      int above = incl - sum;
+#pragma unroll
+      for (int j = 0; j < kBinsPerThread; ++j) {
+        if (above < krem && krem <= above + h[j]) {
+          sc.bin = nb - 1 - kBinsPerThread * tid - j;
+          sc.above = above;
+          sc.in_bin = h[j];
+        }
+        above += h[j];
+      }
+    }
+    __syncthreads();
+    const int bin = sc.bin, above = sc.above;
+    in_bin = sc.in_bin;
+    __syncthreads();
+    krem -= above;
+    n_gt += above;
+    fixed = (fixed << (hib - lob)) | (uint32_t)bin;
+    hib = lob;
+    if (hib == 0) return {kmin + fixed, n_gt, in_bin};  // the bin is one key
+  }
+  // at most kRankDirect keys left in the bin: gather them and rank each
+  // against the others
+  if (tid == 0) sc.n_small = 0;
+  __syncthreads();
+  for (int i = tid; i < count; i += kTkThreads) {
+    const uint32_t key = key_at(i), u = key - kmin;
+    const uint32_t high = hib >= 32 ? 0u : (u >> hib);
+    if (high == fixed) sc.small[atomicAdd(&sc.n_small, 1)] = key;
+  }
+  __syncthreads();
+  if (tid < in_bin) {
+    const uint32_t e = sc.small[tid];
+    int gt = 0, eq = 0;
+    for (int j = 0; j < in_bin; ++j) {
+      const uint32_t o = sc.small[j];
+      gt += o > e;
+      eq += o == e;
+    }
+    if (gt < krem && krem <= gt + eq) {  // every holder of the wanted key writes the same
+      sc.tau = e;
+      sc.gt = gt;
+      sc.eq = eq;
+    }
+  }
+  __syncthreads();
+  const Selection r = {sc.tau, n_gt + sc.gt, sc.eq};
+  __syncthreads();
+  return r;
+}
+
+// Marks the k selected columns of the row in the bitmap bm (zeroed, n bits)
+// and writes them in ascending order to orow.  elem(i) -> (key, column) for
+// i < count enumerates a set holding every element with key >= s.tau.
+template <class Elem>
+__device__ void emit_selection(const Elem &elem, int count, const Selection &s, int k, int n,
+                               uint32_t *bm, int32_t *orow, TkScratch &sc) {
+  const int tid = threadIdx.x;
+  const int need = k - s.n_gt;  // ties to keep, 1..s.n_eq
+  const int nw = (n + 31) >> 5;
+  const int per = (nw + kTkThreads - 1) / kTkThreads;  // contiguous words per thread
+  const int w0 = min(tid * per, nw), w1 = min(w0 + per, nw);
+  if (s.n_eq > need) {
+    // the ties first, cut after the need-th in column order
+    for (int i = tid; i < count; i += kTkThreads) {
+      uint32_t key;
+      int col;
+      elem(i, key, col);
+      if (key == s.tau) atomicOr(&bm[col >> 5], 1u << (col & 31));
+    }
+    __syncthreads();
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
+    const int incl = block_incl_scan(c, sc);
+    if (incl - c < need && need <= incl) {
+      int r = need - 1 - (incl - c);  // rank of the last kept tie among this thread's bits
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = bm[w];
+        const int pc = __popc(m);
+        if (r < pc) {
+          for (int j = 0; j < r; ++j) m &= m - 1;
+          sc.cut = 32 * w + __ffs(m) - 1;
+          break;
+        }
+        r -= pc;
+      }
+    }
+    __syncthreads();
+    const int cut = sc.cut;
+    for (int w = w0; w < w1; ++w) {
+      const int d = cut - 32 * w;  // bits 0..d of word w are kept
+      if (d < 0)
+        bm[w] = 0u;
+      else if (d < 31)
+        bm[w] &= (2u << d) - 1u;
+    }
+    __syncthreads();
+    for (int i = tid; i < count; i += kTkThreads) {
+      uint32_t key;
+      int col;
+      elem(i, key, col);
+      if (key > s.tau) atomicOr(&bm[col >> 5], 1u << (col & 31));
+    }
+  } else {
+    for (int i = tid; i < count; i += kTkThreads) {
+      uint32_t key;
+      int col;
+      elem(i, key, col);
+      if (key >= s.tau) atomicOr(&bm[col >> 5], 1u << (col & 31));
+    }
+  }
+  __syncthreads();
+  int c = 0;
+  for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
+  const int incl = block_incl_scan(c, sc);
+  if (tid == kTkThreads - 1) sc.total = incl;
+  int pos = incl - c;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t m = bm[w];
+    while (m) {
+      if (pos < k) orow[pos] = 32 * w + __ffs(m) - 1;
+      ++pos;
+      m &= m - 1;
+    }
+  }
+  __syncthreads();
+  // exactly k columns are marked; the padding only keeps the row defined if
+  // NaN logits broke the count
+  for (int j = sc.total + tid; j < k; j += kTkThreads) orow[j] = -1;
+}
+
+// One row of the selection (every thread of the block).  next_x / next_n: the
+// CTA's next row, prefetched into L2 once this row no longer needs the
+// filter pass (nullptr: none).
+__device__ __forceinline__ void select_row(const float *__restrict__ x, int n, int k, int cap,
+                                           int32_t *__restrict__ orow, uint32_t *ckey,
+                                           int32_t *ccol, uint32_t *bm, TkScratch &sc,
+                                           const float *next_x, int next_n) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const float4 *x4 = reinterpret_cast<const float4 *>(x);
+  const int nw = (n + 31) >> 5;
+  for (int w = tid; w < nw; w += kTkThreads) bm[w] = 0u;
+
+  bool try_candidates = cap >= k;
+  float c = -INFINITY;
+  if (try_candidates && n > cap) {
+    if (n >= kSample) {
+      // 1. the sample: group tid at a float4 boundary, 8 logits, inside the row
+      const int64_t off = ((int64_t)tid * (n - 8) / (kTkThreads - 1)) & ~(int64_t)3;
+      const float4 a = __ldg(x4 + off / 4), b = __ldg(x4 + off / 4 + 1);
+      const uint32_t sk[8] = {order_key(a.x), order_key(a.y), order_key(a.z), order_key(a.w),
+                              order_key(b.x), order_key(b.y), order_key(b.z), order_key(b.w)};
+      uint32_t lo = sk[0], hi = sk[0];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        ckey[j * kTkThreads + tid] = sk[j];  // (the select ignores the order)
+        lo = min(lo, sk[j]);
+        hi = max(hi, sk[j]);
+      }
+      block_minmax(lo, hi, sc);
+      const float p = (float)k / (float)n;
+      const float want = (float)kSample * p + 3.f * sqrtf((float)kSample * p * (1.f - p)) + 2.f;
+      const int r = min(kSample, max(1, (int)ceilf(want)));
+      const Selection s = block_select([&](int i) { return ckey[i]; }, kSample, r, lo, hi, sc);
+      c = key_value(s.tau);
+    } else {
+      try_candidates = false;
+    }
+  }
+
+  if (try_candidates) {
+    // 2. the filter pass
+    if (tid == 0) sc.cnt = 0;
+    __syncthreads();
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;  // of this thread's candidates
+    const int nv = (n + 3) >> 2;
+    for (int base = 0; base < nv; base += kTkThreads * kFilterUnroll) {
+      float4 v[kFilterUnroll];
+#pragma unroll
+      for (int u = 0; u < kFilterUnroll; ++u) {
+        const int vi = base + u * kTkThreads + tid;
+        v[u] = vi < nv ? __ldcs(x4 + vi) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+      // one ballot per (load, component): the warp's candidates of a slot go to
+      // consecutive entries (lane order), one shared-memory append per warp
+      // (the ballots are taken again for the stores rather than held)
+      int total = 0;
+#pragma unroll
+      for (int u = 0; u < kFilterUnroll; ++u) {
+        const int j = 4 * (base + u * kTkThreads + tid);
+        total += __popc(__ballot_sync(0xffffffffu, j < n && v[u].x >= c)) +
+                 __popc(__ballot_sync(0xffffffffu, j + 1 < n && v[u].y >= c)) +
+                 __popc(__ballot_sync(0xffffffffu, j + 2 < n && v[u].z >= c)) +
+                 __popc(__ballot_sync(0xffffffffu, j + 3 < n && v[u].w >= c));
+      }
+      int wbase = 0;
+      if (lane == 0 && total) wbase = atomicAdd(&sc.cnt, total);
+      int p = __shfl_sync(0xffffffffu, wbase, 0);
+      if (total) {
+        uint32_t lt;
+        asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+#pragma unroll
+        for (int u = 0; u < kFilterUnroll; ++u) {
+          const int j = 4 * (base + u * kTkThreads + tid);
+          const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const bool pass = j + t < n && e[t] >= c;
+            const uint32_t bal = __ballot_sync(0xffffffffu, pass);
+            if (pass) {
+              const uint32_t key = order_key(e[t]);
+              lo = min(lo, key);
+              hi = max(hi, key);
+              const int q = p + __popc(bal & lt);
+              if (q < cap) {
+                ckey[q] = key;
+                ccol[q] = j + t;
+              }
+            }
+            p += __popc(bal);
+          }
+        }
+      }
+    }
+    block_minmax(lo, hi, sc);  // (its first barrier also ends the appends)
+    const int cnt = sc.cnt;
+    // every logit below c ranks below every candidate, so with at least k
+    // candidates the row's top k are among them
+    if (cnt >= k && cnt <= cap) {
+      if (tid == 0 && next_x) prefetch_row_l2(next_x, next_n);
+      // 3.-4. exact selection over the candidates
+      const Selection s = block_select([&](int i) { return ckey[i]; }, cnt, k, lo, hi, sc);
+      emit_selection(
+          [&](int i, uint32_t &key, int &col) {
+            key = ckey[i];
+            col = ccol[i];
+          },
+          cnt, s, k, n, bm, orow, sc);
+      return;
+    }
+  }
+  // the same exact selection over the whole row in global memory
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = tid; i < n; i += kTkThreads) {
+    const uint32_t key = order_key(__ldg(x + i));
+    lo = min(lo, key);
+    hi = max(hi, key);
+  }
+  block_minmax(lo, hi, sc);
+  const Selection s =
+      block_select([&](int i) { return order_key(__ldg(x + i)); }, n, k, lo, hi, sc);
+  if (tid == 0 && next_x) prefetch_row_l2(next_x, next_n);
+  emit_selection(
+      [&](int i, uint32_t &key, int &col) {
+        key = order_key(__ldg(x + i));
+        col = i;
+      },
+      n, s, k, n, bm, orow, sc);
+}
+
+__global__ void __launch_bounds__(kTkThreads, 4)
+    topk_select_kernel(const float *__restrict__ logits, int64_t stride, int n_rows,
+                       const int32_t *__restrict__ row_len, int max_len, int k, int cap,
+                       int32_t *__restrict__ out, int *status) {
+  extern __shared__ __align__(16) uint8_t tk_smem[];
+  __shared__ TkScratch sc;
+  uint32_t *ckey = reinterpret_cast<uint32_t *>(tk_smem);  // max(cap, kSample) keys
+  int32_t *ccol = reinterpret_cast<int32_t *>(ckey + max(cap, kSample));  // cap columns
+  uint32_t *bm = reinterpret_cast<uint32_t *>(ccol + cap);  // ceil(max_len / 32) words
+  const int tid = threadIdx.x;
+
+  // a row's length, -1 for none; out-of-range lengths are recorded and read as 0
+  auto length_of = [&](int i) -> int {
+    if (i >= n_rows) return -1;
+    const int n = row_len[n_rows - 1 - i];
+    if (n < 0 || n > max_len) {
+      if (tid == 0) record_status(status, CPMLA_ERR_INDEX);
+      return 0;
+    }
+    return n;
+  };
+  // rows in reverse (long causal rows sit at the end), in turn over the CTAs
+  int i = blockIdx.x;
+  int n = length_of(i);
+  if (tid == 0 && n > k) prefetch_row_l2(logits + (int64_t)(n_rows - 1 - i) * stride, n);
+  for (; i < n_rows; i += gridDim.x) {
+    const int row = n_rows - 1 - i;
+    int32_t *orow = out + (int64_t)row * k;
+    const int i_next = i + gridDim.x;
+    const int n_next = length_of(i_next);
+    if (n <= k) {
+      for (int j = tid; j < k; j += kTkThreads) orow[j] = j < n ? j : -1;
+    } else {
+      const float *next_x =
+          n_next > k ? logits + (int64_t)(n_rows - 1 - i_next) * stride : nullptr;
+      select_row(logits + (int64_t)row * stride, n, k, cap, orow, ckey, ccol, bm, sc, next_x,
+                 n_next);
+    }
+    if (n <= k && n_next > k && tid == 0)
+      prefetch_row_l2(logits + (int64_t)(n_rows - 1 - i_next) * stride, n_next);
+    n = n_next;
+    __syncthreads();  // shared memory is reused by the next row
+  }
+}
+
+}  // namespace
+}  // namespace cpmla
+
+extern "C" int mla_topk_select(const float *logits, int64_t logits_row_stride, int n_rows,
+                               const int32_t *row_len, int max_row_len, int k,
+                               int32_t *topk_idx, void *stream) {
+  using namespace cpmla;
+  const char *fn = "mla_topk_select";
+  CPMLA_CHECK_ARG(n_rows >= 0, "%s: n_rows=%d < 0", fn, n_rows);
+  CPMLA_CHECK_ARG(k >= 1 && k <= CPMLA_TOPK_MAX, "%s: k=%d outside 1..%d", fn, k, CPMLA_TOPK_MAX);
+  CPMLA_CHECK_ARG(max_row_len >= 0 && max_row_len <= CPMLA_TOPK_MAX_ROW,
+                  "%s: max_row_len=%d outside 0..%d", fn, max_row_len, CPMLA_TOPK_MAX_ROW);
+  CPMLA_CHECK_ARG(logits_row_stride >= max_row_len && logits_row_stride % 4 == 0,
+                  "%s: logits_row_stride=%lld must be >= max_row_len and a multiple of 4", fn,
+                  (long long)logits_row_stride);
+  if (n_rows == 0) return CPMLA_OK;
+  CPMLA_CHECK_ARG(row_len && topk_idx, "%s: row_len and topk_idx are required", fn);
+  CPMLA_CHECK_ARG(max_row_len <= k || (logits && ((uintptr_t)logits & 15) == 0),
+                  "%s: logits must be non-NULL and 16-byte aligned", fn);
+  int *status = status_word();
+  if (!status) return fail(CPMLA_ERR_CUDA, "%s: status word unavailable", fn);
+
+  // candidate capacity: room for the expected k + a few standard deviations
+  const int64_t bm_bytes = 4 * (((int64_t)max_row_len + 31) / 32);
+  // (at least the sample's size, so that every row too short to sample is
+  // taken whole)
+  int64_t cap = std::min<int64_t>(std::max<int64_t>(2 * (int64_t)k + 1024, kSample),
+                                  (kSmemBudget - bm_bytes) / 8);
+  if (cap < kSample)  // the key array still holds the sample
+    cap = std::max<int64_t>(0, std::min<int64_t>(cap, (kSmemBudget - bm_bytes - 4 * kSample) / 4));
+  const size_t smem = 4 * (size_t)std::max<int64_t>(cap, kSample) + 4 * (size_t)cap + (size_t)bm_bytes;
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_topk_select: shared memory attribute");
+  // persistent CTAs: as many as fit on the device at once
+  int dev = 0, n_sm = 0, per_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_select_kernel, kTkThreads, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "mla_topk_select: occupancy");
+  const int64_t grid = std::min<int64_t>(n_rows, (int64_t)std::max(1, n_sm * per_sm));
+  topk_select_kernel<<<(unsigned)grid, kTkThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      logits, logits_row_stride, n_rows, row_len, max_row_len, k, (int)cap, topk_idx, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "mla_topk_select: launch");
+  return CPMLA_OK;
+}

@@ -224,3 +224,27 @@ def attended_keys(prob: Problem) -> int:
     if prob.topk == 0:
         return int((pos + 1).sum())
     return int(torch.clamp(pos + 1, max=prob.topk).sum())
+
+
+# ------------------------------------------------------------ indexer logits
+def indexer_logits(n_rows: int, width: int, *, seed: int = 0, kind: str = "normal",
+                   device="cpu") -> torch.Tensor:
+    """Seeded fp32 [n_rows, width] stand-in for an indexer's scores (trained
+    indexer weights are not available):
+      normal  N(0,1) per entry
+      ties    integers in [-3, 3] (long runs of equal values)
+      mixed   N(0,1) with 10% +0, 5% -0, 5% -inf and 10% copies of one value
+    Drawn on ``device`` with a generator of that device."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    if kind == "ties":
+        return torch.randint(-3, 4, (n_rows, width), generator=gen, device=device).float()
+    x = torch.randn((n_rows, width), generator=gen, device=device)
+    if kind == "mixed":
+        u = torch.rand((n_rows, width), generator=gen, device=device)
+        x[u < 0.10] = 0.0
+        x[(u >= 0.10) & (u < 0.15)] = -0.0
+        x[(u >= 0.15) & (u < 0.20)] = -math.inf
+        x[(u >= 0.20) & (u < 0.30)] = 0.75
+    elif kind != "normal":
+        raise ValueError("unknown logits kind %r" % kind)
+    return x

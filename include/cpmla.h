@@ -268,6 +268,45 @@ int mla_kv_cache_insert(const void *kv, int64_t kv_token_stride, int n,
                         float *cache_scale, void *cache_rope, int64_t s_cache, void *stream);
 
 /* --------------------------------------------------------------------------
+ * 2d. Top-k selection of the indexer's logits (device)
+ *
+ * "[Feat][NVIDIA] DeepSeek-V4.1: Prefill support CP with multistream forward
+ * prepare (4/N)": the sparse attention's key lists come from the indexer,
+ * whose mqa_logits step scores each query token against its request's keys
+ * and whose topk_v2 step keeps the best k.  The pages give no formula for
+ * either; the scores need trained indexer weights, so they are an input here
+ * and this call is the selection.  For row i with m = row_len[i] candidates
+ * logits[i, 0 .. m-1]:
+ *   m <= k : topk_idx[i, :] = 0, 1, .., m-1, then -1
+ *   m >  k : the k columns of the largest values, ordered by the IEEE total
+ *            order of binary32 (-0 below +0), ties to the smaller column,
+ *            written in ascending column order
+ * For a request's query at position t, row_len = t + 1 gives the causal
+ * prefix, and the result is the request-local topk_idx row the sparse
+ * attention (2., 2b.) reads.
+ *
+ * Arguments (device unless noted):
+ *   logits        fp32 [n_rows, logits_row_stride] (the whole extent
+ *                 allocated), 16-byte aligned; never read for rows with
+ *                 row_len <= k.  NaN logits leave the selection unspecified
+ *                 (still k distinct in-range columns).
+ *   logits_row_stride  elements between rows (host), >= max_row_len, a
+ *                 multiple of 4
+ *   n_rows        rows (host); 0 is a no-op
+ *   row_len       int32 [n_rows], each in 0 .. max_row_len
+ *   max_row_len   bound on row_len (host), 0 .. CPMLA_TOPK_MAX_ROW
+ *   k             (host), 1 .. CPMLA_TOPK_MAX
+ *   topk_idx      int32 [n_rows, k] output
+ * A row_len outside 0 .. max_row_len writes an all -1 row and is recorded as
+ * CPMLA_ERR_INDEX in the status word.  Errors: CPMLA_ERR_ARG, CPMLA_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+#define CPMLA_TOPK_MAX 65536
+#define CPMLA_TOPK_MAX_ROW (1 << 20)
+int mla_topk_select(const float *logits, int64_t logits_row_stride, int n_rows,
+                    const int32_t *row_len, int max_row_len, int k, int32_t *topk_idx,
+                    void *stream);
+
+/* --------------------------------------------------------------------------
  * 3. Global LSE merge + attention sink once + restore to global order (device)
  *
  * "[DeepSeekV4][PCP] ...", "Implementation summary" (merge LSE/output

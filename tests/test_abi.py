@@ -37,7 +37,7 @@ def test_exports_every_declared_symbol(lib):
     names = _declared_functions()
     assert {"pcp_dualchunk_partition", "mla_partial_attn_dense", "mla_partial_attn_sparse",
             "lse_merge_with_sink", "mla_attn_dense_merged", "mla_attn_sparse_merged",
-            "mla_kv_cache_insert"} <= set(names)
+            "mla_kv_cache_insert", "mla_topk_select"} <= set(names)
     h = ctypes.CDLL(cpmla.LIB_PATH)
     for n in names:
         assert hasattr(h, n), n
@@ -139,6 +139,19 @@ def test_kv_cache_insert_argument_checks(lib):
     assert f(None, 576, 4, None, 0, None, None, None, None, 0, None) == cpmla.CPMLA_ERR_ARG
     assert f(None, 576, -1, None, 0, None, None, None, None, 16, None) == cpmla.CPMLA_ERR_ARG
     assert b"mla_kv_cache_insert" in lib.cpmla_last_error()
+
+
+def test_topk_select_argument_checks(lib):
+    f = lib.mla_topk_select
+    assert f(None, 64, 0, None, 64, 8, None, None) == cpmla.CPMLA_OK
+    assert f(None, 64, 4, None, 64, 0, None, None) == cpmla.CPMLA_ERR_ARG  # k = 0
+    assert f(None, 64, 4, None, 64, 65537, None, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 62, 4, None, 60, 8, None, None) == cpmla.CPMLA_ERR_ARG  # stride % 4
+    assert f(None, 64, 4, None, 65, 8, None, None) == cpmla.CPMLA_ERR_ARG  # stride < max_row_len
+    assert f(None, 1 << 21, 4, None, (1 << 20) + 1, 8, None, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 64, -1, None, 64, 8, None, None) == cpmla.CPMLA_ERR_ARG
+    assert f(None, 64, 4, None, 64, 8, None, None) == cpmla.CPMLA_ERR_ARG  # row_len NULL
+    assert b"mla_topk_select" in lib.cpmla_last_error()
 
 
 def test_merge_argument_checks(lib):
