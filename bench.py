@@ -36,7 +36,7 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
 NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
-                     ("topk_s8k_k2048", "topk"): 126_343_936 + 8_413_952}
+                     ("topk_s8k_k2048", "topk"): 126_344_960 + 8_766_720}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 

@@ -45,11 +45,10 @@ constexpr int kSmemBudget = 200 * 1024;
 constexpr int kRankDirect = 64;   // a bin this small is finished by direct ranking
 constexpr int kDigitBits = 8;     // radix digit: 256 bins, one per thread in the scan
 constexpr int kBins = 1 << kDigitBits;
-constexpr int kBinsPerThread = kBins / kTkThreads;
 constexpr int kPrefetchChunk = 32768;
 
 static_assert(kSample == 8 * kTkThreads, "one sample group of 8 logits per thread");
-static_assert(kBinsPerThread * kTkThreads == kBins, "whole bins per thread");
+static_assert(kBins == kTkThreads, "one histogram bin per thread when clearing");
 
 // order-preserving image of a binary32 value: unsigned compare of keys is the
 // IEEE total order (-0 below +0)
@@ -76,7 +75,7 @@ __device__ __forceinline__ void prefetch_row_l2(const float *x, int n) {
 }
 
 struct TkScratch {
-  int hist[kBins];
+  int hist[2][kBins];  // double-buffered: one is cleared while the other is scanned
   int wsum[kTkWarps];
   uint32_t rlo[kTkWarps], rhi[kTkWarps];
   int cnt;       // candidates appended by the filter pass
@@ -111,7 +110,9 @@ __device__ __forceinline__ int block_incl_scan(int v, TkScratch &sc) {
   return v + add;
 }
 
-// Smallest and largest of each thread's (lo, hi) over the block.
+// Smallest and largest of each thread's (lo, hi) over the block.  One
+// barrier: the per-warp slots are written again only by a later call, after
+// further barriers.
 __device__ __forceinline__ void block_minmax(uint32_t &lo, uint32_t &hi, TkScratch &sc) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -130,60 +131,74 @@ __device__ __forceinline__ void block_minmax(uint32_t &lo, uint32_t &hi, TkScrat
     lo = min(lo, sc.rlo[w]);
     hi = max(hi, sc.rhi[w]);
   }
-  __syncthreads();
 }
 
 // Radix select of the kth-largest key (1 <= kth <= count) among
-// key_at(0 .. count-1), whose smallest and largest keys are kmin and kmax.
-// Digits of kDigitBits are taken from the top of the keys' range
-// (key - kmin), so the first histogram already spreads over it; once the bin
-// holding the wanted rank has at most kRankDirect keys they are gathered and
-// ranked against each other.  Called by every thread; ends with a barrier.
+// key_at(0 .. count-1); (lo, hi) is each thread's smallest and largest of
+// the keys (the block's are taken here).  Digits of kDigitBits are taken from
+// the top of the keys' range (key - min), so the first histogram already
+// spreads over it; warp 0 scans each histogram while the other warps clear
+// the next one.  Once the bin holding the wanted rank has at most
+// kRankDirect keys they are gathered and ranked against each other.  Called
+// by every thread; ends with a barrier.
 template <class KeyAt>
-__device__ Selection block_select(const KeyAt &key_at, int count, int kth, uint32_t kmin,
-                                  uint32_t kmax, TkScratch &sc) {
-  const int tid = threadIdx.x;
+__device__ Selection block_select(const KeyAt &key_at, int count, int kth, uint32_t lo,
+                                  uint32_t hi, TkScratch &sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  sc.hist[0][tid] = 0;  // kTkThreads == kBins
+  sc.hist[1][tid] = 0;
+  if (tid == 0) sc.n_small = 0;
+  block_minmax(lo, hi, sc);
+  const uint32_t kmin = lo, kmax = hi;
   if (kmin == kmax) return {kmax, 0, count};
 
   int hib = 32 - __clz((int)(kmax - kmin));  // bits hib.. of (key - kmin) are zero
   uint32_t fixed = 0;                          // (key - kmin) >> hib of the wanted element
   int krem = kth, n_gt = 0, in_bin = count;
-  while (in_bin > kRankDirect) {
+  for (int pass = 0; in_bin > kRankDirect; ++pass) {
+    int *hist = sc.hist[pass & 1];
     const int lob = max(hib - kDigitBits, 0), nb = 1 << (hib - lob);
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) sc.hist[tid + j * kTkThreads] = 0;
-    __syncthreads();
     for (int i = tid; i < count; i += kTkThreads) {
       const uint32_t u = key_at(i) - kmin;
       const uint32_t high = hib >= 32 ? 0u : (u >> hib);
-      if (high == fixed) atomicAdd(&sc.hist[(u >> lob) & (uint32_t)(nb - 1)], 1);
+      if (high == fixed) atomicAdd(&hist[(u >> lob) & (uint32_t)(nb - 1)], 1);
     }
     __syncthreads();
-    // bins from the top, kBinsPerThread consecutive ones per thread
-    int h[kBinsPerThread], sum = 0;
+    if (warp == 0) {
+      // bins from the top, 8 consecutive ones per lane (bins >= nb are 0)
+      constexpr int kPer = kBins / 32;
+      int h[kPer], sum = 0;
 #pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) {
-      const int bin = nb - 1 - kBinsPerThread * tid - j;
-      h[j] = bin >= 0 ? sc.hist[bin] : 0;
-      sum += h[j];
-    }
-    const int incl = block_incl_scan(sum, sc);
-    if (incl - sum < krem && krem <= incl) {
-      int above = incl - sum;
-#pragma unroll
-      for (int j = 0; j < kBinsPerThread; ++j) {
-        if (above < krem && krem <= above + h[j]) {
-          sc.bin = nb - 1 - kBinsPerThread * tid - j;
-          sc.above = above;
-          sc.in_bin = h[j];
-        }
-        above += h[j];
+      for (int j = 0; j < kPer; ++j) {
+        h[j] = hist[kBins - 1 - kPer * lane - j];
+        sum += h[j];
       }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (incl - sum < krem && krem <= incl) {
+        int above = incl - sum;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          if (above < krem && krem <= above + h[j]) {
+            sc.bin = kBins - 1 - kPer * lane - j;
+            sc.above = above;
+            sc.in_bin = h[j];
+          }
+          above += h[j];
+        }
+      }
+    } else {
+      // the other buffer was scanned in the previous pass and is next used
+      // after the barrier below
+      for (int i = tid - 32; i < kBins; i += kTkThreads - 32) sc.hist[(pass + 1) & 1][i] = 0;
     }
     __syncthreads();
     const int bin = sc.bin, above = sc.above;
     in_bin = sc.in_bin;
-    __syncthreads();
     krem -= above;
     n_gt += above;
     fixed = (fixed << (hib - lob)) | (uint32_t)bin;
@@ -192,8 +207,6 @@ __device__ Selection block_select(const KeyAt &key_at, int count, int kth, uint3
   }
   // at most kRankDirect keys left in the bin: gather them and rank each
   // against the others
-  if (tid == 0) sc.n_small = 0;
-  __syncthreads();
   for (int i = tid; i < count; i += kTkThreads) {
     const uint32_t key = key_at(i), u = key - kmin;
     const uint32_t high = hib >= 32 ? 0u : (u >> hib);
@@ -215,9 +228,7 @@ __device__ Selection block_select(const KeyAt &key_at, int count, int kth, uint3
     }
   }
   __syncthreads();
-  const Selection r = {sc.tau, n_gt + sc.gt, sc.eq};
-  __syncthreads();
-  return r;
+  return {sc.tau, n_gt + sc.gt, sc.eq};
 }
 
 // Marks the k selected columns of the row in the bitmap bm (zeroed, n bits)
@@ -328,7 +339,6 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
         lo = min(lo, sk[j]);
         hi = max(hi, sk[j]);
       }
-      block_minmax(lo, hi, sc);
       const float p = (float)k / (float)n;
       const float want = (float)kSample * p + 3.f * sqrtf((float)kSample * p * (1.f - p)) + 2.f;
       const int r = min(kSample, max(1, (int)ceilf(want)));
@@ -393,7 +403,7 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
         }
       }
     }
-    block_minmax(lo, hi, sc);  // (its first barrier also ends the appends)
+    __syncthreads();
     const int cnt = sc.cnt;
     // every logit below c ranks below every candidate, so with at least k
     // candidates the row's top k are among them
@@ -417,7 +427,6 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
     lo = min(lo, key);
     hi = max(hi, key);
   }
-  block_minmax(lo, hi, sc);
   const Selection s =
       block_select([&](int i) { return order_key(__ldg(x + i)); }, n, k, lo, hi, sc);
   if (tid == 0 && next_x) prefetch_row_l2(next_x, next_n);
