@@ -362,21 +362,22 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
         const int vi = base + u * kTkThreads + tid;
         v[u] = vi < nv ? __ldcs(x4 + vi) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
-      // one ballot per (load, component): the warp's candidates of a slot go to
-      // consecutive entries (lane order), one shared-memory append per warp
-      // (the ballots are taken again for the stores rather than held)
-      int total = 0;
+      // this thread's candidates; a whole iteration inside the row needs no
+      // bounds checks
+      const bool whole = 4 * (base + kTkThreads * kFilterUnroll) <= n;
+      int q = 0;
 #pragma unroll
       for (int u = 0; u < kFilterUnroll; ++u) {
         const int j = 4 * (base + u * kTkThreads + tid);
-        total += __popc(__ballot_sync(0xffffffffu, j < n && v[u].x >= c)) +
-                 __popc(__ballot_sync(0xffffffffu, j + 1 < n && v[u].y >= c)) +
-                 __popc(__ballot_sync(0xffffffffu, j + 2 < n && v[u].z >= c)) +
-                 __popc(__ballot_sync(0xffffffffu, j + 3 < n && v[u].w >= c));
+        q += (int)((whole || j < n) && v[u].x >= c) + (int)((whole || j + 1 < n) && v[u].y >= c) +
+             (int)((whole || j + 2 < n) && v[u].z >= c) + (int)((whole || j + 3 < n) && v[u].w >= c);
       }
+      const int total = __reduce_add_sync(0xffffffffu, q);
       int wbase = 0;
       if (lane == 0 && total) wbase = atomicAdd(&sc.cnt, total);
       int p = __shfl_sync(0xffffffffu, wbase, 0);
+      // one ballot per (load, component): the warp's candidates of a slot go to
+      // consecutive entries (lane order), one shared-memory append per warp
       if (total) {
         uint32_t lt;
         asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
@@ -386,16 +387,16 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
           const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const bool pass = j + t < n && e[t] >= c;
+            const bool pass = (whole || j + t < n) && e[t] >= c;
             const uint32_t bal = __ballot_sync(0xffffffffu, pass);
             if (pass) {
               const uint32_t key = order_key(e[t]);
               lo = min(lo, key);
               hi = max(hi, key);
-              const int q = p + __popc(bal & lt);
-              if (q < cap) {
-                ckey[q] = key;
-                ccol[q] = j + t;
+              const int at = p + __popc(bal & lt);
+              if (at < cap) {
+                ckey[at] = key;
+                ccol[at] = j + t;
               }
             }
             p += __popc(bal);
