@@ -113,3 +113,27 @@ def test_full_size_causal_32k_sampled_rows():
     ti = torch.as_tensor(rows, device="cuda")
     want = orc.topk_select(x[ti].cpu().numpy(), rl[ti].cpu().numpy(), k)
     assert np.array_equal(got[ti].cpu().numpy(), want)
+
+
+def test_selected_lists_drive_the_sparse_attention():
+    """The index producer feeding the sparse attention: lists selected from
+    seeded logits (varlen requests with decode rows, request-local causal
+    prefixes) are the oracle's, and the sparse path run on them matches the
+    oracle's attention over the same lists."""
+    from tests import parity_util as pu
+    prob = synth.make_problem("varlen_p8_h64", prefill_lens=[2500, 700, 3], decode_ctx=[3000, 40],
+                              H=16, P=4, topk=512, device="cuda", seed=9)
+    pos = prob.token_pos()
+    row_len = (pos + 1).to(torch.int32)
+    width = (int(row_len.max()) + 3) // 4 * 4
+    x = synth.indexer_logits(prob.T, width, seed=10, device="cuda")
+    idx = cpmla.mla_topk_select(x, row_len.cuda(), prob.topk)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    want = orc.topk_select(x.cpu().numpy(), row_len.numpy(), prob.topk)
+    assert np.array_equal(idx.cpu().numpy(), want)
+    prob.idx = idx
+    o, lse, _ = pu.run_path(prob)
+    toks = np.arange(prob.T)
+    ro, rl = pu.oracle_tokens(prob, toks)
+    pu.compare(o, lse, ro, rl)
