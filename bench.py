@@ -35,7 +35,8 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472}
+NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
+                     ("topk_s8k_k2048", "topk"): 126_344_192 + 8_175_360}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
