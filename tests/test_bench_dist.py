@@ -40,3 +40,31 @@ def test_two_gloo_ranks_take_the_slowest_rank():
         t, thr = res[rank]
         assert t == pytest.approx(15.0)
         assert thr == pytest.approx(world * 1000.0 / 15e-3)
+
+
+def test_topk_algorithmic_bytes_count_rows_longer_than_k():
+    """The top-k line's byte count: rows longer than k read their logits,
+    every row reads its length and writes k indices."""
+    import bench
+    rl = torch.tensor([1, 5, 8, 9, 100], dtype=torch.int32)
+    assert bench.rows_bytes(rl, 8) == 4 * (9 + 100) + 4 * 5 + 4 * 5 * 8
+    n = torch.arange(1, 8193, dtype=torch.int64)
+    assert bench.rows_bytes(n.to(torch.int32), 2048) == (
+        4 * int(n[n > 2048].sum()) + 4 * 8192 + 4 * 8192 * 2048)
+
+
+def test_topk_reference_arm_prints_its_line():
+    """bench.py --impl reference on the 8192-row top-k workload runs the
+    oracle on host cores and prints one JSON line of the contract."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "topk_s8k_k2048", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
