@@ -22,8 +22,7 @@
  *     merged globally by LSE and the attention sink is applied once, after
  *     the merge, never per shard.
  *
- * Readings taken where the pages are silent (listed with reasons in the
- * design notes of the repository):
+ * Readings taken where the pages are silent (labels used below):
  *   R1 sink = one extra logit per head, zero value vector, same units as the
  *      scaled scores: O_final = O * e^L / (e^L + e^sink).
  *   R3 returned LSE is natural-log and excludes the sink.

@@ -209,9 +209,12 @@ def kv_insert(kv_bits, slot, *, fmt, s_cache, cache=None):
     """Insert tokens' latent KV (bf16 bits [n, 576]) into cache rows slot[t]
     (-1 skips), bf16 (fmt 0) or fp8 (fmt 1; per-128-channel amax/448 scales,
     E4M3 codes), as "[Core] Add MRV2 virtual-batch PCP for MLA" inserts the
-    all-gathered latent KV into the cache; the quantisation rule is the
-    reading R13 of the repository's design notes.  `cache` (dict of numpy
-    arrays) is updated in place and returned; fresh zero arrays if None."""
+    all-gathered latent KV into the cache.  The pages give no quantisation
+    rule; this one is the library's: per group scale = amax / 448 in
+    binary32 (1 for an all-zero group), code = E4M3(x / scale) with the
+    quotient in binary32, nearest-even, saturating at +-448.  `cache` (dict
+    of numpy arrays) is updated in place and returned; fresh zero arrays if
+    None."""
     lib = _load()
     kv = _c(kv_bits, np.uint16)
     n = kv.shape[0]
@@ -236,8 +239,9 @@ def topk_select(logits, row_len, k):
     0 .. row_len[i]-1, the k largest values -- ties to the smaller column --
     returned as column indices in ascending order, -1 padded; a row with at
     most k candidates returns all of them.  Values are ordered by the IEEE
-    total order of non-NaN binary32 (-0 below +0), the reading R14 of the
-    repository's design notes.  logits: float32 [n_rows, >= max(row_len)].
+    total order of non-NaN binary32 (-0 below +0); the pages give no tie
+    rule, so ties go to the smaller column, which makes the selected set
+    unique.  logits: float32 [n_rows, >= max(row_len)].
     Returns int32 [n_rows, k]."""
     x = np.asarray(logits, dtype=np.float32)
     lens = np.asarray(row_len, dtype=np.int64)

@@ -1,6 +1,6 @@
 """Pins of the oracle's top-k selection (the indexer's topk step of "[Feat]
 [NVIDIA] DeepSeek-V4.1: Prefill support CP with multistream forward prepare
-(4/N)"; the selection rule is the reading R14 of the design notes): brute
+(4/N)"; the pages give no tie rule, so ties go to the smaller column): brute
 force over all k-subsets on tiny rows, ties to the smaller column, the
 signed-zero order, short rows, and the result being a valid top-k."""
 import itertools
