@@ -42,7 +42,7 @@ enum {
   CPMLA_OK = 0,
   CPMLA_ERR_ARG = -1,         /* bad argument (null, size, alignment, range) */
   CPMLA_ERR_CUDA = -2,        /* a CUDA runtime call or launch failed */
-  CPMLA_ERR_UNSUPPORTED = -3, /* valid request this build does not implement */
+  CPMLA_ERR_UNSUPPORTED = -3, /* valid request the library does not implement */
   CPMLA_ERR_TIMEOUT = -4,     /* status word: a bounded device wait ran out */
   CPMLA_ERR_INDEX = -5        /* status word: an index outside its row's range */
 };
