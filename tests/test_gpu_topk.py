@@ -137,3 +137,15 @@ def test_selected_lists_drive_the_sparse_attention():
     toks = np.arange(prob.T)
     ro, rl = pu.oracle_tokens(prob, toks)
     pu.compare(o, lse, ro, rl)
+
+
+def test_maximum_row_length():
+    # rows of up to 2^20 columns: a 128 KB column bitmap per CTA
+    w = 1 << 20
+    _case([w, w - 3, 5000, 0], w, 2048, "normal", 11)
+
+
+def test_maximum_k_takes_the_whole_row_path():
+    # k = 65536 exceeds the candidate buffer, so every row longer than k is
+    # selected over the row in global memory
+    _case([70000, 65536, 65537, 100], 70000, 65536, "normal", 12)
