@@ -64,11 +64,16 @@ __global__ void __launch_bounds__(kMergeThreads)
     float acc[kVecPerLane * 4];
 #pragma unroll
     for (int i = 0; i < kVecPerLane * 4; ++i) acc[i] = 0.f;
-    // L = max + ln sum exp(lse_c - max) over the valid partials
+    // L = max + ln sum exp(lse_c - max) over the valid partials; a contrib
+    // row outside [0, n_part) is skipped and recorded here, before anything
+    // else depends on it (also when it is the token's only partial)
     float mx = -INFINITY;
     for (int c = c0; c < c1; ++c) {
       const int r = contrib_rows[c];
-      if (r < 0 || (int64_t)r >= n_part) continue;
+      if (r < 0 || (int64_t)r >= n_part) {
+        if (lane == 0) record_status(status, CPMLA_ERR_INDEX);
+        continue;
+      }
       mx = fmaxf(mx, lse_part[(int64_t)r * H + h]);
     }
     float L = -INFINITY;
@@ -82,10 +87,7 @@ __global__ void __launch_bounds__(kMergeThreads)
       L = mx + logf(z);
       for (int c = c0; c < c1; ++c) {
         const int r = contrib_rows[c];
-        if (r < 0 || (int64_t)r >= n_part) {
-          if (lane == 0) record_status(status, CPMLA_ERR_INDEX);
-          continue;
-        }
+        if (r < 0 || (int64_t)r >= n_part) continue;
         const float l = lse_part[(int64_t)r * H + h];
         if (l == -INFINITY) continue;
         const float w = expf(l - L);

@@ -2,12 +2,13 @@
 run the fp64 oracle on chosen global tokens, and compare with the stated
 tolerances.
 
-O: |d| <= 1e-2 * max(1, |O_ref|) per element and mean |d| <= 1e-3; LSE:
-|d| <= 1e-3.  The O bounds are stated for unit-scale outputs.  The output is
-bf16, whose own rounding of a value of magnitude m can reach m * 2^-8 (0.0156
-for m in [4, 8)), so rows with very few keys -- whose O is close to a single
-value row, up to ~4.5 for N(0,1) data -- get the bound scaled by their
-magnitude.  Elements with |O_ref| <= 1 keep the absolute 1e-2."""
+O: |d| <= 1e-2 + 2^-8 * |O_ref| per element and mean |d| <= 1e-3; LSE:
+|d| <= 1e-3.  The absolute 1e-2 is the stated bound for unit-scale outputs;
+the output is bf16, whose own rounding of a value of magnitude m reaches
+m * 2^-8 (half a unit in the last place of an 8-bit significand), so each
+element may also carry its own rounding on top of it.  Rows with very few
+keys have O close to a single value row (up to ~4.5 for N(0,1) data, ~10 for
+the fp8 cache's scaled values), which is where that term matters."""
 import numpy as np
 import torch
 
@@ -15,6 +16,7 @@ from context_sparse_mla_gb300 import cpmla
 from oracle import oracle as orc
 
 O_MAX, O_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
+O_REL = 2.0 ** -8  # bf16 output rounding of the element itself
 
 
 def run_path(prob):
@@ -58,12 +60,12 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref):
     dl = np.abs(lg - lse_ref)
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lg), fin), "LSE finiteness differs"
-    scaled = d / np.maximum(1.0, np.abs(o_ref))
-    stats = dict(o_max=float(d.max()), o_max_scaled=float(scaled.max()), o_mean=float(d.mean()),
+    excess = d - O_REL * np.abs(o_ref)  # what is left after the element's own rounding
+    stats = dict(o_max=float(d.max()), o_max_excess=float(excess.max()), o_mean=float(d.mean()),
                  o_max_unit=float(d[np.abs(o_ref) <= 1.0].max()) if (np.abs(o_ref) <= 1).any()
                  else 0.0,
                  lse_max=float(dl[fin].max()) if fin.any() else 0.0)
-    assert stats["o_max_scaled"] <= O_MAX, stats
+    assert stats["o_max_excess"] <= O_MAX, stats
     assert stats["o_mean"] <= O_MEAN, stats
     assert stats["lse_max"] <= LSE_MAX, stats
     return stats
