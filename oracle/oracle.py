@@ -116,6 +116,84 @@ def partition(P: int, cu_seqlens, q_start_pos, is_decode):
     return out
 
 
+def ratio2_linkage(P: int, cu_seqlens, q_start_pos, is_decode):
+    """Predecessor-row linkage of a ratio-2 compressor across DualChunkSwap
+    chunks ("[Feature][PCP] Add DeepSeek-V4.1-Flash support", sections
+    "Overview" and "Implementation": ratio-2 groups are compressed on each
+    rank's local token rows, and the pairs split across PCP chunks are closed
+    with gathered predecessor rows -- only the last row of each local chunk is
+    gathered; "Rank-local Compressor Revision" names the cases: PCP2/4
+    linkage, replicated short prefills, empty ranks, request isolation and
+    the newest open ring rows).
+
+    Readings where the page is silent: a ratio-2 group is the pair of request
+    positions (2m, 2m+1); chunk sizes, chunk order and shard assignment are
+    those of the partition (first S mod 2P chunks one token larger; shard r
+    holds chunks r and 2P-1-r); decode requests (replicated, one row) have no
+    chunks and no entries.
+
+    One entry per (shard r, prefill request b in input order, local chunk k:
+    k = 0 is chunk r, k = 1 is chunk 2P-1-r), shard-major.  For a chunk
+    holding request positions p0 .. p1 (global tokens first .. last):
+      first, last  its first and last global token (-1, -1 when empty)
+      flags bit 0  p0 is odd: the pair (p0-1, p0) straddles the chunk's start
+            bit 1  ... and position p0-1 was scheduled in an earlier step (the
+                   request's open ring row), not in this batch
+            bit 2  p1 is even: the pair (p1, p1+1) is open at the chunk's end
+            bit 3  ... and p1 is the request's last scheduled token, so that
+                   row is the request's newest open ring row
+      pred         global token of position p0-1 when bit 0 is set and that
+                   position is in this batch (the last token of the nearest
+                   earlier non-empty chunk of the same request), else -1
+      pred_shard   the shard whose local chunk holds pred, else -1
+    Returns a dict of int32 arrays (first, last, pred, pred_shard, flags)."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    qs = np.asarray(q_start_pos, dtype=np.int64)
+    dec = np.asarray(is_decode, dtype=np.int64)
+    B = len(cu) - 1
+    nch = 2 * P
+
+    def chunk(S, c):  # start and length of chunk c of an S-token request
+        base, rem = divmod(S, nch)
+        return c * base + min(c, rem), base + (1 if c < rem else 0)
+
+    def shard_of(c):
+        return c if c < P else nch - 1 - c
+
+    out = {k: [] for k in ("first", "last", "pred", "pred_shard", "flags")}
+    for r in range(P):
+        for b in range(B):
+            if dec[b]:
+                continue
+            g0, S, q0 = int(cu[b]), int(cu[b + 1] - cu[b]), int(qs[b])
+            for c in (r, nch - 1 - r):
+                st, ln = chunk(S, c)
+                first = last = pred = pshard = -1
+                flags = 0
+                if ln > 0:
+                    first, last = g0 + st, g0 + st + ln - 1
+                    p0, p1 = q0 + st, q0 + st + ln - 1
+                    if p0 % 2 == 1:
+                        flags |= 1
+                        if st >= 1:
+                            # local index st-1 lies in the nearest earlier
+                            # non-empty chunk of this request
+                            cp = max(cc for cc in range(c) if chunk(S, cc)[1] > 0)
+                            pred, pshard = g0 + st - 1, shard_of(cp)
+                        else:
+                            flags |= 2
+                    if p1 % 2 == 0:
+                        flags |= 4
+                        if st + ln == S:
+                            flags |= 8
+                out["first"].append(first)
+                out["last"].append(last)
+                out["pred"].append(pred)
+                out["pred_shard"].append(pshard)
+                out["flags"].append(flags)
+    return {k: np.asarray(v, dtype=np.int32) for k, v in out.items()}
+
+
 def attention(q_bits, pos, kv_start, *, kv_bf16=None, kv_fp8=None, kv_scale=None,
               kv_rope=None, topk=None, kv_lo=None, kv_hi=None, scale, sink=None):
     """Plain definition of (partial) attention for n query rows, all heads
