@@ -45,6 +45,9 @@ _SIGS = {
                                     _P, _P, _P, _I, _F, _P, _I, _P, _P, _P, _P]),
     "mla_kv_cache_insert": (_I, [_P, _I64, _I, _P, _I, _P, _P, _P, _P, _I64, _P]),
     "mla_topk_select": (_I, [_P, _I64, _I, _P, _I, _I, _P, _P]),
+    "pcp_ratio2_linkage_size": (_I, [_I, _I, _P, _P, _P]),
+    "pcp_ratio2_linkage": (_I, [_I, _I] + [_P] * 8),
+    "pcp_gather_rows_f32": (_I, [_P, _I64, _I64, _I, _I, _P, _P, _I64, _P]),
 }
 
 _lock = threading.Lock()
@@ -119,6 +122,36 @@ def pcp_dualchunk_partition(P, cu_seqlens, q_start_pos, is_decode):
     _check(L.pcp_dualchunk_partition(P, B, _ptr(cu), _ptr(qs), _ptr(dec),
                                      *[_ptr(out[k]) for k in ("shard_offsets", "rows", "pos",
                                                               "req", "owner_shard", "owner_row")]))
+    return out
+
+
+def pcp_ratio2_linkage(P, cu_seqlens, q_start_pos, is_decode):
+    """Host ratio-2 linkage across DualChunkSwap chunks; returns a dict of
+    int32 numpy arrays (first, last, pred, pred_shard, flags), one entry per
+    (shard, prefill request, local chunk), shard-major."""
+    L = lib()
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    qs = np.ascontiguousarray(np.asarray(q_start_pos, dtype=np.int32))
+    dec = np.ascontiguousarray(np.asarray(is_decode, dtype=np.uint8))
+    B = len(cu) - 1
+    n = ctypes.c_int64(0)
+    _check(L.pcp_ratio2_linkage_size(P, B, _ptr(cu), _ptr(dec), ctypes.byref(n)))
+    keys = ("first", "last", "pred", "pred_shard", "flags")
+    out = {k: np.zeros(n.value, np.int32) for k in keys}
+    _check(L.pcp_ratio2_linkage(P, B, _ptr(cu), _ptr(qs), _ptr(dec), *[_ptr(out[k]) for k in keys]))
+    return out
+
+
+def pcp_gather_rows_f32(src, idx, out=None, *, stream=None):
+    """out[i] = src[idx[i]] (fp32 rows, zeros where idx[i] == -1) on the GPU."""
+    _dev(src, torch.float32, "src")
+    _dev(idx, torch.int32, "idx")
+    n_src, D = src.shape
+    if out is None:
+        out = torch.empty((idx.numel(), D), dtype=torch.float32, device=src.device)
+    _dev(out, torch.float32, "out")
+    _check(lib().pcp_gather_rows_f32(_ptr(src), src.stride(0), n_src, D, idx.numel(), _ptr(idx),
+                                     _ptr(out), out.stride(0), _stream(stream)))
     return out
 
 

@@ -125,6 +125,60 @@ int pcp_dualchunk_partition(int P, int B, const int32_t *cu_seqlens, const int32
                             int32_t *owner_row);
 
 /* --------------------------------------------------------------------------
+ * 1b. Ratio-2 compressor linkage across chunks (host) and the gather of the
+ *     linked rows (device)
+ *
+ * "[Feature][PCP] Add DeepSeek-V4.1-Flash support", "Overview" and
+ * "Implementation": ratio-2 groups are compressed on each rank's local token
+ * rows; a pair split across two PCP chunks is closed with the preceding
+ * chunk's last row, and only the last (fp32) row of each local chunk is
+ * gathered.  "Rank-local Compressor Revision" names the cases: PCP2/4 linkage,
+ * replicated short prefills, empty ranks, request isolation and the newest
+ * open ring rows.  Readings where the page is silent: a ratio-2 group is the
+ * pair of request positions (2m, 2m+1); chunks are those of
+ * pcp_dualchunk_partition; decode requests have no chunks and no entries.
+ * The compressor's combining arithmetic is not on the pages and not here.
+ *
+ * pcp_ratio2_linkage_size: n_links = 2 * P * (number of prefill requests).
+ * pcp_ratio2_linkage (host; inputs as for pcp_dualchunk_partition): one entry
+ * per (shard r, prefill request in input order, local chunk h), shard-major,
+ * h = 0 for chunk r and h = 1 for chunk 2P-1-r.  For a chunk holding request
+ * positions p0 .. p1, global tokens first .. last (all [n_links], int32):
+ *   first, last  the chunk's first and last global token, -1 when empty
+ *   pred         global token at position p0-1 when p0 is odd and that
+ *                position is in this batch (the last token of the nearest
+ *                earlier non-empty chunk of the same request), else -1
+ *   pred_shard   the shard holding pred, else -1
+ *   flags        bit 0: p0 is odd (the pair (p0-1, p0) straddles the start);
+ *                bit 1: ... and p0-1 was scheduled in an earlier step (the
+ *                request's open ring row); bit 2: p1 is even (the pair (p1,
+ *                p1+1) is open at the end); bit 3: ... and p1 is the
+ *                request's last scheduled token (its newest open ring row)
+ * Errors: CPMLA_ERR_ARG (null pointer, P outside 1..1024, decreasing offsets,
+ * negative position).
+ *
+ * pcp_gather_rows_f32 (device): out[i, 0:D] = src[idx[i], 0:D] for
+ * i < n, zeros where idx[i] == -1 -- with idx = pred, each chunk's
+ * predecessor row out of the rows all shards share on one GPU (the gathered
+ * last rows; with idx = last, the gathered buffer itself).
+ *   src    fp32 [n_src, src_row_stride], out fp32 [n, out_row_stride]; both
+ *          16-byte aligned, strides (elements) >= D and multiples of 4
+ *   D      row width, a positive multiple of 4
+ *   idx    int32 [n]; an index outside [-1, n_src) zeroes its row and is
+ *          recorded as CPMLA_ERR_INDEX in the status word
+ * Errors: CPMLA_ERR_ARG, CPMLA_ERR_CUDA.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+int pcp_ratio2_linkage_size(int P, int B, const int32_t *cu_seqlens, const uint8_t *is_decode,
+                            int64_t *n_links);
+
+int pcp_ratio2_linkage(int P, int B, const int32_t *cu_seqlens, const int32_t *q_start_pos,
+                       const uint8_t *is_decode, int32_t *first, int32_t *last, int32_t *pred,
+                       int32_t *pred_shard, int32_t *flags);
+
+int pcp_gather_rows_f32(const float *src, int64_t src_row_stride, int64_t n_src, int D, int n,
+                        const int32_t *idx, float *out, int64_t out_row_stride, void *stream);
+
+/* --------------------------------------------------------------------------
  * 2. Per-shard partial MLA attention (device)
  *
  * "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
