@@ -125,14 +125,17 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
     args.g = 64 / args.hc;
     R = 64;
   } else {
-    // fp8 works on 16 heads at a time (its split-P region is sized for R = 16)
-    const int hmax = kv_format == CPMLA_KV_FP8_E4M3_G128 ? 16 : 32;
+    // one token per CTA.  fp8 works on 16 heads at a time (its split-P
+    // region is sized for R = 16); bf16 takes up to 16 heads in the narrow
+    // kernel, up to 32 or 64 in the wide one (all heads of a 64-head token in
+    // one CTA, so its keys are gathered once)
+    const int hmax = kv_format == CPMLA_KV_FP8_E4M3_G128 ? 16 : 64;
     args.hc = H <= hmax ? H : hmax;
     if (H > hmax && H % hmax != 0)
       return fail(CPMLA_ERR_UNSUPPORTED, "%s: H=%d > %d must be a multiple of %d", fn, H, hmax,
                   hmax);
     args.g = 1;
-    R = args.hc <= 16 ? 16 : 32;
+    R = args.hc <= 16 ? 16 : (args.hc <= 32 ? 32 : 64);
   }
   args.n_hgroups = H / args.hc;
   const int64_t n_groups = (n_rows + args.g - 1) / args.g;
@@ -173,6 +176,8 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
     }
     if (cr2 != CUDA_SUCCESS)
       return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr2);
+    if (kv_format == CPMLA_KV_BF16 && R > 16)
+      return launch_sparse_wide(R, args, tm_kv, (int)n_items, st);
     return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args, tm_kv,
                          tm_rope, (int)n_items, st);
   }

@@ -157,5 +157,9 @@ int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cu
 // tm_rope = the bf16 rope (box 64 x 1, 128-byte swizzle).
 int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
                   const CUtensorMap &tm_rope, int n_items, cudaStream_t st);
+// Sparse, bf16 KV, R = 32 or 64 heads per CTA (attn_sparse_wide.cu); tm_kv as
+// for the bf16 narrow kernel.
+int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
+                       cudaStream_t st);
 
 }  // namespace cpmla

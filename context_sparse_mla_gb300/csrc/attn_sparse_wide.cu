@@ -1,0 +1,706 @@
+// attn_sparse_wide.cu -- top-k sparse partial MLA attention (output + LSE, no
+// sink) over a bf16 latent KV for 17 to 64 heads of one token per CTA, on
+// sm_103a.
+//
+// "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
+// MegaMoE", "Implementation summary": each shard computes the partial
+// attention of its query rows over their own top-k keys, merged later by LSE
+// (or, for a token's single owner row, in this kernel's epilogue).
+//
+// One CTA = one token x R heads (R = 32 or 64).  A token's keys are its own,
+// so every gathered key row feeds only this token's heads: with R = 64 one
+// CTA covers all heads of a 64-head token and each key row is gathered once.
+//   * Score GEMM key-major: S^T = K . Q^T, M = 128 keys, N = R, K = 576, into
+//     one of two TMEM buffers.  PV GEMM: O^T += V^T . P^T, M = 128 dv x 4
+//     chunks, N = R, K = 128 keys, V read from the k-blocks the score GEMM
+//     used (the latent is the value, so it stays resident).
+//   * Shared memory: Q [R x 576], P^T [128 keys x R], a ring of NP 32 KB pair
+//     slots (two k-blocks [128 keys x 64 dims]); pair p of tile j at ring
+//     position 4j + p.  R = 32: a rope slot of its own and five pair slots, so
+//     the next tile's first pair lands while the current tile's four are in
+//     use.  R = 64 (Q alone is 72 KB): four pair slots, and the rope k-block
+//     shares the region of P^T -- the rope of tile j+1 is gathered once the
+//     PV GEMM of tile j has read P^T, and the score GEMM takes the rope last.
+//   * The gathers are issued by the softmax warps.  A tile's slots are freed
+//     by the PV GEMM that follows its softmax, and the next tile's softmax
+//     needs those slots gathered first, so these warps would otherwise be
+//     idle exactly when the gathers are due.  Eight warps issue TMA four-row
+//     gathers (tile::gather4; one warp's lanes issue one after another, so the
+//     gather rate grows with the number of issuing warps): warp w fills key
+//     quarter w % 4 of k-block w / 4 of every pair slot, and keys 16w..16w+15
+//     of the rope.
+//   * Warp 0 issues the score GEMMs, warps 1 and 2 the PV GEMMs (dv chunks 0,
+//     2 and 1, 3): one thread issues an MMA only every ~80 cycles, about the
+//     tensor core's time for an N = 64 MMA.  Warp 3 resolves each tile's key
+//     rows into shared memory a tile ahead.
+//   * Softmax: two warpgroups (warps 4-7 and 8-11) take R/2 score columns
+//     each; thread i = TMEM lane i = key i of the tile (dv i of an O^T chunk).
+//     Base 2, with a row reference moved only when a score passes it by 2^8.
+//   * Every wait is bounded; a wait that decides a warpgroup's control flow is
+//     taken by one thread and published to the group, so the group's named
+//     barriers always match.  On expiry the CTA records CPMLA_ERR_TIMEOUT,
+//     drains its copies and MMAs, frees TMEM and exits.
+#include <cmath>
+
+#include "attn_common.cuh"
+
+namespace cpmla {
+namespace {
+
+constexpr int kWThreads = 384;       // 12 warps
+constexpr int kWMetaWarp = 3;        // key-row resolution
+constexpr int kWGroup0 = 4;          // softmax + gather warps 4..11
+constexpr int kWGatherWarps = 8;
+constexpr int kWSlotBytes = 2 * kKbBytes;  // 32 KB pair slot
+constexpr int kWPairs = 4;                 // latent k-block pairs per tile
+constexpr int kWRec = 6;                   // gathers remembered per warp for the drain
+
+template <int R>
+struct WideCfg {
+  static_assert(R == 32 || R == 64, "32 or 64 heads per CTA");
+  static constexpr int RC = R / 2;                   // score columns per softmax warpgroup
+  static constexpr bool kRopeInP = R == 64;          // rope shares the P^T region
+  static constexpr int kPBytes = kTileKeys * R * 2;  // P^T [128 keys x R]
+  static constexpr int kPRegion = kRopeInP ? kKbBytes : kPBytes;
+  static constexpr int kRopeSlot = kRopeInP ? 0 : kKbBytes;
+  static constexpr int kQBytes = R * CPMLA_DQK * 2;
+  static constexpr uint32_t kTmemCols = 2 * R + 4 * R <= 256 ? 256 : 512;
+};
+static_assert(WideCfg<64>::kPBytes == kKbBytes, "rope k-block and P^T have one size");
+
+template <int R>
+struct WideCtrl {
+  uint64_t full[8];       // pair slot landed: one arrival per gather warp
+  uint64_t empty[8];      // pair slot released by its PV GEMM chunk
+  uint64_t rope_full;     // rope landed: one arrival per gather warp
+  uint64_t rope_empty;    // separate rope slot read by the score GEMM
+  uint64_t s_full[2];
+  uint64_t s_free[2];     // S^T buffer read: every softmax thread
+  uint64_t p_full;        // P^T written: every softmax thread
+  uint64_t p_free;        // PV GEMM of a tile done: both PV issuers
+  uint64_t o_full;        // all PV GEMMs done: both PV issuers
+  uint64_t drain[3];      // per MMA-issuing thread
+  uint64_t meta_full[2];  // key rows of a tile written: the meta warp's 32 lanes
+  uint64_t meta_empty[2]; // key rows of a tile no longer needed: every softmax thread
+  uint32_t tmem_base;
+  int abort;
+  int last_slot;          // setup: the largest non-empty top-k slot of the row
+  int row_ok;             // setup: the row's token may be read
+  int gtok;               // merged output: the global token this CTA writes, or -1
+  int bflag[2][2];        // elected wait results per warpgroup, alternating
+  int pf_ok[2];
+  int need_rescale[2];
+  int key_row[2][kTileKeys];  // KV row of each key of a tile, -1 = masked
+  float red[2][4][32];
+  float m_ref[R];
+  float alpha[R];
+  float lse[R];
+  float inv_l[R];
+  float sfac[R];  // merged output: sink factor per head
+};
+
+template <int R>
+__host__ __device__ constexpr int wide_fixed_bytes() {
+  return 1024 + WideCfg<R>::kQBytes + WideCfg<R>::kPRegion + WideCfg<R>::kRopeSlot +
+         (int)sizeof(WideCtrl<R>);
+}
+template <int R>
+__host__ __device__ constexpr int wide_slots() {
+  return (232448 - wide_fixed_bytes<R>()) / kWSlotBytes > 8
+             ? 8
+             : (232448 - wide_fixed_bytes<R>()) / kWSlotBytes;
+}
+template <int R>
+__host__ __device__ constexpr int wide_smem_bytes() {
+  return wide_fixed_bytes<R>() + wide_slots<R>() * kWSlotBytes;
+}
+
+constexpr unsigned long long kWDrainLimitNs = 20ull * 1000 * 1000;
+__device__ __forceinline__ void wide_drain_wait(uint64_t *bar, uint32_t parity,
+                                                unsigned long long limit_ns) {
+  unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity) && global_timer_ns() - t0 < limit_ns) {
+  }
+}
+
+// MERGED: the epilogue writes the token's merged result (AttnArgs::o_out)
+// instead of the partial (o_part / lse_part).
+template <int R, bool MERGED>
+__global__ void __launch_bounds__(kWThreads, 1)
+    mla_sparse_wide_kernel(const __grid_constant__ AttnArgs a,
+                           const __grid_constant__ CUtensorMap tm_kv) {
+  using Cfg = WideCfg<R>;
+  constexpr int RC = Cfg::RC;
+  constexpr int NP = wide_slots<R>();
+  static_assert(NP >= kWPairs, "a tile needs four pair slots");
+  static_assert(!Cfg::kRopeInP || NP == kWPairs, "the rope-in-P^T order assumes four slots");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *sQ = smem;                                 // 9 k-blocks of [R x 64] bf16
+  uint8_t *sP = sQ + Cfg::kQBytes;                    // P^T (R = 64: also the rope)
+  uint8_t *sRope = Cfg::kRopeInP ? sP : sP + Cfg::kPRegion;  // [128 keys x 64 dims]
+  uint8_t *sRing = sP + Cfg::kPRegion + Cfg::kRopeSlot;      // NP pair slots
+  WideCtrl<R> &c = *reinterpret_cast<WideCtrl<R> *>(sRing + NP * kWSlotBytes);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int item = blockIdx.x;
+  const int row = item / a.n_hgroups;  // one shard row (token) per CTA
+  const int hg = item - row * a.n_hgroups;
+  const int h0 = hg * a.hc;
+  const int r_valid = a.hc;
+
+  // ------------------------------------------------------------ setup
+  if (tid == 0) {
+    for (int s = 0; s < NP; ++s) {
+      mbar_init(&c.full[s], kWGatherWarps);
+      mbar_init(&c.empty[s], 1);
+    }
+    mbar_init(&c.rope_full, kWGatherWarps);
+    mbar_init(&c.rope_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&c.s_full[s], 1);
+      mbar_init(&c.s_free[s], 256);
+      mbar_init(&c.meta_full[s], 32);
+      mbar_init(&c.meta_empty[s], 256);
+    }
+    mbar_init(&c.p_full, 256);
+    mbar_init(&c.p_free, 2);
+    mbar_init(&c.o_full, 2);
+    for (int s = 0; s < 3; ++s) mbar_init(&c.drain[s], 1);
+    c.abort = 0;
+    c.last_slot = -1;
+    c.need_rescale[0] = c.need_rescale[1] = 0;
+    fence_mbar_init();
+  }
+  if (tid == 32) {
+    // the row's token; merged: whether the row owns it (a replicated decode
+    // row is computed in every shard and owned by one).  A token outside
+    // [0, T) is recorded and the row is treated as empty.
+    int ok = row < a.n_rows ? 1 : 0;
+    int gt = -1;
+    if (ok && MERGED) {
+      const int g = a.rows[row];
+      if (g < 0 || g >= a.T) {
+        record_status(a.status, CPMLA_ERR_INDEX);
+        ok = 0;
+      } else if (a.owner_row[g] == row) {
+        gt = g;
+      }
+    }
+    c.row_ok = ok;
+    c.gtok = gt;
+  }
+  if (warp == 0) tmem_alloc(&c.tmem_base, Cfg::kTmemCols);
+  if (warp == kWGroup0 && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (tid < R) {
+    c.m_ref[tid] = -INFINITY;
+    c.alpha[tid] = 1.f;
+  }
+  __syncthreads();
+  const bool row_ok = c.row_ok != 0;
+  const int64_t gq = row_ok ? (int64_t)a.rows[row] : -1;
+  {
+    // the last non-empty slot of the token's list: every thread scans its
+    // share (the loads are independent), one shared atomic each
+    if (row_ok) {
+      const int32_t *lst = a.topk + gq * a.k;
+      int last = -1;
+      for (int e = tid; e < a.k; e += kWThreads)
+        if (__ldg(lst + e) >= 0) last = e;
+      if (last >= 0) atomicMax(&c.last_slot, last);
+    }
+    // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero
+    // padding rows), every thread's loads before its stores
+    constexpr int kChunks = R * (CPMLA_DQK / 8);
+    constexpr int kPer = (kChunks + kWThreads - 1) / kWThreads;
+    uint4 v[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kWThreads;
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (idx < kChunks && r < r_valid && gq >= 0)
+        v[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + gq * a.q_stride +
+                                                     (int64_t)(h0 + r) * CPMLA_DQK) +
+                     ch);
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int idx = tid + k * kWThreads;
+      if (idx >= kChunks) continue;
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      const int kb = ch >> 3, cc = ch & 7;
+      *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v[k];
+    }
+  }
+  fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  const int n_tiles = (c.last_slot + kTileKeys) / kTileKeys;
+  const uint32_t tO = tmem + 2 * R;  // O^T chunk ch at tO + ch*R; S^T buffer b at tmem + b*R
+  volatile int *abort = &c.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------- score-GEMM issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(128, R, 0, 0);
+      // descriptors advance by (byte offset >> 4) in their address field
+      const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
+      const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
+      const uint64_t drope = smem_desc(smem_u32(sRope), 16, 1024, kSwz128);
+      const uint64_t dq_rope = dq0 + ((kLatKb * (R * 128)) >> 4);
+      bool ok = true;
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const uint32_t dS = tmem + (i & 1) * R;
+        if (i >= 2 && !mbar_wait(&c.s_free[i & 1], ((i >> 1) - 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        if (!Cfg::kRopeInP) {
+          // the rope first (it starts the accumulator), then its slot is free
+          if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+            mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_qk,
+                        st == 0 ? 0u : 1u);
+          mma_commit(&c.rope_empty);
+        }
+        for (int p = 0; p < kWPairs; ++p) {
+          const uint32_t pos = 4u * i + p, slot = pos % NP;
+          if (!mbar_wait(&c.full[slot], (pos / NP) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = dr0 + ((slot * kWSlotBytes) >> 4);
+          const uint64_t db = dq0 + ((2 * p * (R * 128)) >> 4);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t h = k >> 2, st = k & 3;
+            mma_bf16_ss(dS, da + ((h * kKbBytes + st * 32) >> 4),
+                        db + ((h * (R * 128) + st * 32) >> 4), id_qk,
+                        (!Cfg::kRopeInP || (p | k) != 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
+        if (Cfg::kRopeInP) {
+          // the rope last: it sits in the P^T region, free only once the PV
+          // GEMM of the previous tile has read P^T
+          if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int st = 0; st < 4; ++st)
+            mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_qk, 1u);
+        }
+        mma_commit(&c.s_full[i & 1]);
+      }
+      if (!ok) {
+        mma_commit(&c.drain[0]);
+        wide_drain_wait(&c.drain[0], 0, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    // ---------------------------------------------------- PV-GEMM issuers
+    // O^T chunk ch += V^T . P^T from tile j's resident pair ch, which is then
+    // released; issuer `me` takes chunks me and me + 2
+    if (lane == 0) {
+      const int me = warp - 1;
+      constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
+      const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 8 * PLayout<R>::row_bytes,
+                                     PLayout<R>::swz);
+      const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int ch = me; ch < kWPairs; ch += 2) {
+          const uint32_t slot = (4u * j + ch) % NP;
+          const uint64_t da = dr0 + ((slot * kWSlotBytes) >> 4);
+#pragma unroll
+          for (int st = 0; st < kTileKeys / 16; ++st)
+            mma_bf16_ss(tO + ch * R, da + ((st * 2048) >> 4),
+                        dp0 + ((st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
+                        (j > 0 || st > 0) ? 1u : 0u);
+          mma_commit(&c.empty[slot]);
+        }
+        mma_commit(&c.p_free);
+      }
+      mma_commit(&c.o_full);
+      if (!ok) {
+        mma_commit(&c.drain[1 + me]);
+        wide_drain_wait(&c.drain[1 + me], 0, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWMetaWarp) {
+    // ---------------------------------------------------- key rows
+    // key t of tile j: its KV row, or -1 when the slot is empty or outside
+    // the row's range; the list entries of tile j+1 load while tile j's are
+    // resolved
+    if (row_ok && n_tiles > 0) {
+      const int tpos = a.pos[row];
+      const int64_t base = a.kv_start[a.req[row]];
+      const int32_t *lst = a.topk + gq * a.k;
+      const int lo = a.kv_lo ? a.kv_lo[row] : 0;
+      const int hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
+      int nxt[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e = q * 32 + lane;
+        nxt[q] = e < a.k ? __ldg(lst + e) : -1;
+      }
+      for (int j = 0; j < n_tiles; ++j) {
+        int cur[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          cur[q] = nxt[q];
+          const int e = (j + 1) * kTileKeys + q * 32 + lane;
+          nxt[q] = (j + 1 < n_tiles && e < a.k) ? __ldg(lst + e) : -1;
+        }
+        // the softmax of tile j-2 (and with it every gather of that tile)
+        // must be done with this buffer
+        if (j >= 2) {
+          int okw = 1;
+          if (lane == 0)
+            okw = mbar_wait(&c.meta_empty[j & 1], ((j >> 1) - 1) & 1, abort, a.status) ? 1 : 0;
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) break;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int p = cur[q];
+          int src = -1;
+          if (p >= 0) {
+            if (p > tpos || base + p >= a.s_kv)
+              record_status(a.status, CPMLA_ERR_INDEX);
+            else if (p >= lo && p <= hi)
+              src = (int)(base + p);
+          }
+          c.key_row[j & 1][q * 32 + lane] = src;
+        }
+        mbar_arrive(&c.meta_full[j & 1]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------- softmax + gathers
+    const int gw = warp - kWGroup0;  // gather warp 0..7
+    const int grp = gw >> 2;         // softmax warpgroup
+    const int q4 = gw & 3;           // TMEM lane quarter
+    const int t = tid - kWGroup0 * 32 - grp * 128;  // key of a tile / dv of a chunk
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int cbase = grp * RC;
+    const int bar_id = 1 + grp;
+    int seq = 0;
+    bool ok = true;
+    float l_part[RC];
+#pragma unroll
+    for (int r = 0; r < RC; ++r) l_part[r] = 0.f;
+    // the last gathers this warp issued, drained if the CTA gives up
+    uint64_t *rec_bar[kWRec];
+    uint32_t rec_par[kWRec];
+    int n_rec = 0;
+
+    // My share of one gather unit.  Pair slot: key quarter q4 of k-block
+    // (gw >> 2) = 32 keys x 64 dims (8 four-row gathers); rope: keys 16 gw ..
+    // 16 gw + 15 (4 gathers).  A masked key fetches KV row 0, which the
+    // softmax gives weight exactly 0.
+    auto gather = [&](bool rope, int tile, int pr, uint8_t *dst, uint64_t *bar, uint32_t par) {
+      const int *krow = c.key_row[tile & 1];
+      const int k0 = rope ? 16 * gw : 32 * q4;
+      const int n4 = rope ? 4 : 8;
+      uint8_t *d = rope ? dst + gw * 2048 : dst + (gw >> 2) * kKbBytes + q4 * 4096;
+      const int x = rope ? CPMLA_DV : pr * 128 + (gw >> 2) * kKbDims;
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n4 * 512);
+      __syncwarp();
+      if (lane < n4) {
+        const int *kr = krow + k0 + 4 * lane;
+        tma_gather4(d + lane * 512, &tm_kv, x, kr[0] >= 0 ? kr[0] : 0, kr[1] >= 0 ? kr[1] : 0,
+                    kr[2] >= 0 ? kr[2] : 0, kr[3] >= 0 ? kr[3] : 0, bar);
+      }
+      rec_bar[n_rec % kWRec] = bar;
+      rec_par[n_rec % kWRec] = par;
+      ++n_rec;
+    };
+
+    // Softmax of tile j for this warpgroup's columns; false when the CTA
+    // gave up.
+    auto softmax = [&](int j) -> bool {
+      const int sb = j & 1;
+      if (!group_wait(&c.s_full[sb], (j >> 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
+                      a.status))
+        return false;
+      tc_fence_after();
+      const uint32_t tS = tmem + sb * R + lane_off + cbase;
+      float s[RC];
+#pragma unroll
+      for (int cc = 0; cc < RC / 16; ++cc) tmem_ld16(tS + cc * 16, s + cc * 16);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&c.s_free[sb]);  // the next-but-one score GEMM may overwrite it
+      {
+        const bool valid = c.key_row[sb][t] >= 0;
+#pragma unroll
+        for (int r = 0; r < RC; ++r)
+          s[r] = (valid && cbase + r < r_valid) ? s[r] * a.scale_log2 : -INFINITY;
+      }
+      // PV(j-1) must be done before P^T is overwritten or O^T rescaled:
+      // thread 0 waits, the barrier below publishes its result
+      if (t == 0)
+        c.pf_ok[grp] = (j == 0 || mbar_wait(&c.p_free, (j - 1) & 1, abort, a.status)) ? 1 : 0;
+      // the reference of a row moves only when a score passes it by more than
+      // 2^8 (always on its first finite score); otherwise no row maxima
+      bool over = false;
+#pragma unroll
+      for (int r = 0; r < RC; ++r) over |= s[r] > c.m_ref[cbase + r] + 8.f;
+      const bool move = named_bar_or(bar_id, 128, over);
+      if (!*reinterpret_cast<volatile int *>(&c.pf_ok[grp])) return false;
+      if (move) {
+        {
+          float v[RC];
+#pragma unroll
+          for (int r = 0; r < RC; ++r) v[r] = s[r];
+          warp_transpose_reduce<RC, true>(v, lane);
+          if (RC == 32 || (lane & 1) == 0) c.red[grp][q4][RC == 32 ? lane : (lane >> 1)] = v[0];
+        }
+        named_bar_sync(bar_id, 128);
+        if (t < RC) {
+          const int r = cbase + t;
+          const float tile_max = fmaxf(fmaxf(c.red[grp][0][t], c.red[grp][1][t]),
+                                       fmaxf(c.red[grp][2][t], c.red[grp][3][t]));
+          const float m_old = c.m_ref[r];
+          float m_new = m_old;
+          if (tile_max > m_old + 8.f) m_new = tile_max;  // lazy move of the reference
+          c.alpha[r] = (m_old == -INFINITY) ? 0.f : fast_exp2(m_old - m_new);
+          c.m_ref[r] = m_new;
+          if (j > 0 && m_new != m_old) c.need_rescale[grp] = j + 1;
+        }
+        named_bar_sync(bar_id, 128);
+      }
+      const bool rescale = move && c.need_rescale[grp] == j + 1;
+      uint32_t pk[RC / 2];
+#pragma unroll
+      for (int r = 0; r < RC; r += 2) {
+        const float m0 = c.m_ref[cbase + r], m1 = c.m_ref[cbase + r + 1];
+        const float p0 = fast_exp2(s[r] - (m0 == -INFINITY ? 0.f : m0));
+        const float p1 = fast_exp2(s[r + 1] - (m1 == -INFINITY ? 0.f : m1));
+        pk[r / 2] = pack_bf16x2(p0, p1);
+        if (move) {
+          l_part[r] = l_part[r] * c.alpha[cbase + r] + p0;
+          l_part[r + 1] = l_part[r + 1] * c.alpha[cbase + r + 1] + p1;
+        } else {
+          l_part[r] += p0;
+          l_part[r + 1] += p1;
+        }
+      }
+      tc_fence_after();
+      if (rescale) {
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+          for (int cc = 0; cc < RC / 16; ++cc) {
+            float o[16];
+            const uint32_t col = tO + lane_off + ch * R + cbase + cc * 16;
+            tmem_ld16(col, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) o[x] *= c.alpha[cbase + cc * 16 + x];
+            tmem_st16(col, o);
+          }
+        }
+        tmem_st_wait();
+      }
+      // P^T row of key t: this group's RC columns, 16-byte chunks swizzled
+      uint8_t *prow = sP + t * PLayout<R>::row_bytes;
+#pragma unroll
+      for (int ch = 0; ch < RC / 8; ++ch) {
+        const int phys = (grp * (RC / 8) + ch) ^ PLayout<R>::chunk_xor(t);
+        *reinterpret_cast<uint4 *>(prow + phys * 16) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&c.p_full);
+      mbar_arrive(&c.meta_empty[sb]);  // done with this tile's key rows
+      return true;
+    };
+
+    // The gather sequence: ring positions in order (R = 32: each tile's rope
+    // before its pair 0; R = 64: after its pair 3).  Position p reuses the
+    // slot of position p - NP, released by the PV GEMM of that tile, which
+    // needs that tile's softmax: softmaxes are taken as the sequence reaches
+    // them, so no wait can depend on work this warpgroup has not done.
+    int next_sm = 0;
+    const int total = 4 * n_tiles;
+    for (int p = 0; p < total && ok; ++p) {
+      const int j = p >> 2, pr = p & 3;
+      if (pr == 0) {
+        if (!group_wait(&c.meta_full[j & 1], (j >> 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
+                        a.status)) {
+          ok = false;
+          break;
+        }
+        if (!Cfg::kRopeInP) {
+          // the rope slot: read by the score GEMM of tile j-1 first
+          if (j >= 1 && !group_wait(&c.rope_empty, (j - 1) & 1, t, bar_id, c.bflag[grp], seq,
+                                    abort, a.status)) {
+            ok = false;
+            break;
+          }
+          gather(true, j, 0, sRope, &c.rope_full, j & 1);
+        }
+      }
+      if (p >= NP) {
+        const int q = p - NP, jq = q >> 2;
+        while (ok && next_sm <= jq) ok = softmax(next_sm++);
+        if (!ok) break;
+        if (!group_wait(&c.empty[p % NP], (q / NP) & 1, t, bar_id, c.bflag[grp], seq, abort,
+                        a.status)) {
+          ok = false;
+          break;
+        }
+      }
+      gather(false, j, pr, sRing + (p % NP) * kWSlotBytes, &c.full[p % NP], (p / NP) & 1);
+      if (Cfg::kRopeInP && pr == 3) {
+        // the rope of tile j goes to the P^T region once PV(j-1) is done
+        if (j >= 1) {
+          while (ok && next_sm <= j - 1) ok = softmax(next_sm++);
+          if (!ok) break;
+          if (!group_wait(&c.p_free, (j - 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
+                          a.status)) {
+            ok = false;
+            break;
+          }
+        }
+        gather(true, j, 0, sRope, &c.rope_full, j & 1);
+      }
+    }
+    while (ok && next_sm < n_tiles) ok = softmax(next_sm++);
+    if (!ok && lane == 0) {
+      // gathers of this warp that may still be landing; a phase another warp
+      // never completed gives up after the short limit
+      for (int m = n_rec > kWRec ? n_rec - kWRec : 0; m < n_rec; ++m)
+        wide_drain_wait(rec_bar[m % kWRec], rec_par[m % kWRec], kWDrainLimitNs);
+    }
+    __syncwarp();
+
+    // ------------------------------------------------ epilogue
+    if (ok) ok = group_wait(&c.o_full, 0, t, bar_id, c.bflag[grp], seq, abort, a.status);
+    if (ok) {
+      tc_fence_after();
+      warp_transpose_reduce<RC, false>(l_part, lane);
+      if (RC == 32 || (lane & 1) == 0) c.red[grp][q4][RC == 32 ? lane : (lane >> 1)] = l_part[0];
+      named_bar_sync(bar_id, 128);
+      if (t < RC) {
+        const int r = cbase + t;
+        const float l = c.red[grp][0][t] + c.red[grp][1][t] + c.red[grp][2][t] + c.red[grp][3][t];
+        const float m = c.m_ref[r];
+        const bool empty = !(l > 0.f) || m == -INFINITY;
+        c.lse[r] = empty ? -INFINITY : (m + __log2f(l)) * 0.69314718055994530942f;
+        c.inv_l[r] = empty ? 0.f : 1.f / l;
+        if (r < r_valid && row_ok) {
+          if (!MERGED) {
+            a.lse_part[(int64_t)row * a.H + h0 + r] = c.lse[r];
+          } else if (c.gtok >= 0) {
+            c.sfac[r] = sink_factor(a.sink, h0 + r, c.lse[r]);
+            a.lse_out[(int64_t)c.gtok * a.H + h0 + r] = c.lse[r];
+          }
+        }
+      }
+      named_bar_sync(bar_id, 128);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int cc = 0; cc < RC / 16; ++cc) {
+          float o[16];
+          if (n_tiles > 0) {
+            tmem_ld16(tO + lane_off + ch * R + cbase + cc * 16, o);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) o[x] = 0.f;
+          }
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const int r = cbase + cc * 16 + x;
+            if (r >= r_valid || !row_ok) continue;
+            if (!MERGED) {
+              a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
+                  o[x] * c.inv_l[r];
+            } else if (c.gtok >= 0) {
+              // merged: stage bf16 rows [head][dv] in the idle ring, stored below
+              reinterpret_cast<__nv_bfloat16 *>(sRing)[r * CPMLA_DV + ch * 128 + t] =
+                  __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
+            }
+          }
+        }
+      }
+    }
+    if (MERGED) {
+      // the token's heads h0 .. h0 + r_valid - 1 are one contiguous span of
+      // o_out: one bulk copy of the staged rows once both warpgroups are here
+      // (both always arrive, also after an abort, which skips the copy)
+      fence_proxy_async_smem();
+      named_bar_sync(3, 256);
+      if (grp == 0 && t == 0 && !*abort && c.gtok >= 0) {
+        bulk_store_s2g(a.o_out + ((int64_t)c.gtok * a.H + h0) * CPMLA_DV, sRing,
+                       (uint32_t)r_valid * CPMLA_DV * 2);
+        bulk_commit();
+        bulk_wait_read();
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int R, bool MERGED>
+int launch_wide_t(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
+                  cudaStream_t stream) {
+  constexpr int smem = wide_smem_bytes<R>();
+  static_assert(smem <= 232448, "shared memory budget");
+  auto kern = mla_sparse_wide_kernel<R, MERGED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention: set shared memory size");
+  kern<<<n_items, kWThreads, smem, stream>>>(args, tm_kv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention: launch");
+  return CPMLA_OK;
+}
+
+}  // namespace
+
+int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
+                       cudaStream_t st) {
+  if (args.o_out)
+    return R == 64 ? launch_wide_t<64, true>(args, tm_kv, n_items, st)
+                   : launch_wide_t<32, true>(args, tm_kv, n_items, st);
+  return R == 64 ? launch_wide_t<64, false>(args, tm_kv, n_items, st)
+                 : launch_wide_t<32, false>(args, tm_kv, n_items, st);
+}
+
+}  // namespace cpmla
