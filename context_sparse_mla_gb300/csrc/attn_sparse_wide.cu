@@ -17,29 +17,33 @@
 //   * Shared memory: Q [R x 576], P^T [128 keys x R], a ring of NP 32 KB pair
 //     slots (two k-blocks [128 keys x 64 dims]); pair p of tile j at ring
 //     position 4j + p.  R = 32: a rope slot of its own and five pair slots, so
-//     the next tile's first pair lands while the current tile's four are in
-//     use.  R = 64 (Q alone is 72 KB): four pair slots, and the rope k-block
-//     shares the region of P^T -- the rope of tile j+1 is gathered once the
-//     PV GEMM of tile j has read P^T, and the score GEMM takes the rope last.
-//   * The gathers are issued by the softmax warps.  A tile's slots are freed
-//     by the PV GEMM that follows its softmax, and the next tile's softmax
-//     needs those slots gathered first, so these warps would otherwise be
-//     idle exactly when the gathers are due.  Eight warps issue TMA four-row
-//     gathers (tile::gather4; one warp's lanes issue one after another, so the
-//     gather rate grows with the number of issuing warps): warp w fills key
-//     quarter w % 4 of k-block w / 4 of every pair slot, and keys 16w..16w+15
-//     of the rope.
+//     the rope and first pair of tile j+2 are gathered while tile j+1 still
+//     waits for its softmax.  R = 64 (Q alone is 72 KB): four pair slots, and
+//     the rope k-block shares the region of P^T -- the rope of tile j+1 is
+//     gathered once the PV GEMM of tile j has read P^T, and the score GEMM
+//     takes the rope last.
+//   * Gathers: TMA four-row gathers (tile::gather4, 512 B each) issued by the
+//     16 softmax warps.  One gather takes a warp ~100-200 cycles to issue, so
+//     an SM's gather rate grows with the number of issuing warps (measured:
+//     23 B/clk with 8, 42 with 16, 49 with 20); and a tile's slots are freed
+//     by the PV GEMM that follows its softmax, so the softmax warps are idle
+//     exactly when the next tile's gathers are due.  Warp w of the 16 fills
+//     keys 16 (w % 8) .. +15 of k-block w / 8 of every pair slot, and keys
+//     8 w .. 8 w + 7 of the rope.  Each warp waits for its slots on its own.
 //   * Warp 0 issues the score GEMMs, warps 1 and 2 the PV GEMMs (dv chunks 0,
 //     2 and 1, 3): one thread issues an MMA only every ~80 cycles, about the
 //     tensor core's time for an N = 64 MMA.  Warp 3 resolves each tile's key
 //     rows into shared memory a tile ahead.
-//   * Softmax: two warpgroups (warps 4-7 and 8-11) take R/2 score columns
-//     each; thread i = TMEM lane i = key i of the tile (dv i of an O^T chunk).
-//     Base 2, with a row reference moved only when a score passes it by 2^8.
-//   * Every wait is bounded; a wait that decides a warpgroup's control flow is
-//     taken by one thread and published to the group, so the group's named
-//     barriers always match.  On expiry the CTA records CPMLA_ERR_TIMEOUT,
-//     drains its copies and MMAs, frees TMEM and exits.
+//   * Softmax: four warpgroups (warps 4-7, 8-11, 12-15, 16-19) take R/4 score
+//     columns each; thread i = TMEM lane i = key i of the tile (dv i of an O^T
+//     chunk).  Base 2, with a row reference moved only when a score passes it
+//     by 2^8.  Per tile the warps run the softmax first, then the gathers it
+//     unblocks.
+//   * Every wait is bounded.  A wait that decides a warpgroup's control flow
+//     is taken by one thread and published to the group, so the group's named
+//     barriers always match; a gather warp whose own wait gives up stops
+//     gathering.  On expiry the CTA records CPMLA_ERR_TIMEOUT, drains its
+//     copies and MMAs, frees TMEM and exits.
 #include <cmath>
 
 #include "attn_common.cuh"
@@ -47,10 +51,12 @@
 namespace cpmla {
 namespace {
 
-constexpr int kWThreads = 384;       // 12 warps
+constexpr int kWThreads = 640;       // 20 warps
 constexpr int kWMetaWarp = 3;        // key-row resolution
-constexpr int kWGroup0 = 4;          // softmax + gather warps 4..11
-constexpr int kWGatherWarps = 8;
+constexpr int kWGroup0 = 4;          // softmax + gather warps 4..19
+constexpr int kWGroups = 4;          // softmax warpgroups
+constexpr int kWGatherWarps = 16;
+constexpr int kWSoftmaxThreads = 128 * kWGroups;
 constexpr int kWSlotBytes = 2 * kKbBytes;  // 32 KB pair slot
 constexpr int kWPairs = 4;                 // latent k-block pairs per tile
 constexpr int kWRec = 6;                   // gathers remembered per warp for the drain
@@ -58,7 +64,7 @@ constexpr int kWRec = 6;                   // gathers remembered per warp for th
 template <int R>
 struct WideCfg {
   static_assert(R == 32 || R == 64, "32 or 64 heads per CTA");
-  static constexpr int RC = R / 2;                   // score columns per softmax warpgroup
+  static constexpr int RC = R / kWGroups;            // score columns per softmax warpgroup
   static constexpr bool kRopeInP = R == 64;          // rope shares the P^T region
   static constexpr int kPBytes = kTileKeys * R * 2;  // P^T [128 keys x R]
   static constexpr int kPRegion = kRopeInP ? kKbBytes : kPBytes;
@@ -87,11 +93,11 @@ struct WideCtrl {
   int last_slot;          // setup: the largest non-empty top-k slot of the row
   int row_ok;             // setup: the row's token may be read
   int gtok;               // merged output: the global token this CTA writes, or -1
-  int bflag[2][2];        // elected wait results per warpgroup, alternating
-  int pf_ok[2];
-  int need_rescale[2];
+  int bflag[kWGroups][2];  // elected wait results per warpgroup, alternating
+  int pf_ok[kWGroups];
+  int need_rescale[kWGroups];
   int key_row[2][kTileKeys];  // KV row of each key of a tile, -1 = masked
-  float red[2][4][32];
+  float red[kWGroups][4][32];
   float m_ref[R];
   float alpha[R];
   float lse[R];
@@ -162,17 +168,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
     mbar_init(&c.rope_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.s_full[s], 1);
-      mbar_init(&c.s_free[s], 256);
+      mbar_init(&c.s_free[s], kWSoftmaxThreads);
       mbar_init(&c.meta_full[s], 32);
-      mbar_init(&c.meta_empty[s], 256);
+      mbar_init(&c.meta_empty[s], kWSoftmaxThreads);
     }
-    mbar_init(&c.p_full, 256);
+    mbar_init(&c.p_full, kWSoftmaxThreads);
     mbar_init(&c.p_free, 2);
     mbar_init(&c.o_full, 2);
     for (int s = 0; s < 3; ++s) mbar_init(&c.drain[s], 1);
     c.abort = 0;
     c.last_slot = -1;
-    c.need_rescale[0] = c.need_rescale[1] = 0;
+    for (int g = 0; g < kWGroups; ++g) c.need_rescale[g] = 0;
     fence_mbar_init();
   }
   if (tid == 32) {
@@ -402,15 +408,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------- softmax + gathers
-    const int gw = warp - kWGroup0;  // gather warp 0..7
+    const int gw = warp - kWGroup0;  // gather warp 0..15
     const int grp = gw >> 2;         // softmax warpgroup
-    const int q4 = gw & 3;           // TMEM lane quarter
-    const int t = tid - kWGroup0 * 32 - grp * 128;  // key of a tile / dv of a chunk
+    const int q4 = warp & 3;         // TMEM lane quarter this warp may access
+    const int t = q4 * 32 + lane;    // key of a tile / dv of a chunk
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const int cbase = grp * RC;
     const int bar_id = 1 + grp;
+    constexpr int kSpread = 32 / RC;  // lanes sharing one column after a reduction
     int seq = 0;
-    bool ok = true;
+    bool ok = true;   // the warpgroup goes on (decided group-wide)
+    bool gok = true;  // this warp's gathers go on (false once one of its waits gave up)
     float l_part[RC];
 #pragma unroll
     for (int r = 0; r < RC; ++r) l_part[r] = 0.f;
@@ -419,16 +427,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
     uint32_t rec_par[kWRec];
     int n_rec = 0;
 
-    // My share of one gather unit.  Pair slot: key quarter q4 of k-block
-    // (gw >> 2) = 32 keys x 64 dims (8 four-row gathers); rope: keys 16 gw ..
-    // 16 gw + 15 (4 gathers).  A masked key fetches KV row 0, which the
-    // softmax gives weight exactly 0.
+    // Per-warp bounded wait (lane 0 waits, the warp takes its result).
+    auto wwait = [&](uint64_t *bar, uint32_t parity) {
+      int r = 1;
+      if (lane == 0) r = mbar_wait(bar, parity, abort, a.status) ? 1 : 0;
+      gok = __shfl_sync(0xffffffffu, r, 0) != 0;
+    };
+    // My share of one gather unit.  Pair slot: keys 16 (gw % 8) .. +15 of
+    // k-block gw / 8 (4 four-row gathers); rope: keys 8 gw .. 8 gw + 7 (2).
+    // A masked key fetches KV row 0, which the softmax gives weight exactly 0.
     auto gather = [&](bool rope, int tile, int pr, uint8_t *dst, uint64_t *bar, uint32_t par) {
       const int *krow = c.key_row[tile & 1];
-      const int k0 = rope ? 16 * gw : 32 * q4;
-      const int n4 = rope ? 4 : 8;
-      uint8_t *d = rope ? dst + gw * 2048 : dst + (gw >> 2) * kKbBytes + q4 * 4096;
-      const int x = rope ? CPMLA_DV : pr * 128 + (gw >> 2) * kKbDims;
+      const int k0 = rope ? 8 * gw : 16 * (gw & 7);
+      const int n4 = rope ? 2 : 4;
+      uint8_t *d = rope ? dst + gw * 1024 : dst + (gw >> 3) * kKbBytes + (gw & 7) * 2048;
+      const int x = rope ? CPMLA_DV : pr * 128 + (gw >> 3) * kKbDims;
       if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n4 * 512);
       __syncwarp();
       if (lane < n4) {
@@ -436,9 +449,32 @@ __global__ void __launch_bounds__(kWThreads, 1)
         tma_gather4(d + lane * 512, &tm_kv, x, kr[0] >= 0 ? kr[0] : 0, kr[1] >= 0 ? kr[1] : 0,
                     kr[2] >= 0 ? kr[2] : 0, kr[3] >= 0 ? kr[3] : 0, bar);
       }
+      __syncwarp();
       rec_bar[n_rec % kWRec] = bar;
       rec_par[n_rec % kWRec] = par;
       ++n_rec;
+    };
+    // Pair pr of tile j into its ring slot, once the slot's previous use has
+    // been released by its PV GEMM (that tile's softmax is always done by
+    // the time this is called).
+    auto gather_pair = [&](int j, int pr) {
+      const int p = 4 * j + pr;
+      if (gok && p >= NP) wwait(&c.empty[p % NP], ((p - NP) / NP) & 1);
+      if (gok) gather(false, j, pr, sRing + (p % NP) * kWSlotBytes, &c.full[p % NP], (p / NP) & 1);
+    };
+    auto gather_meta = [&](int j) {
+      if (gok) wwait(&c.meta_full[j & 1], (j >> 1) & 1);
+    };
+    // rope of tile j: its own slot (R = 32; read first by the score GEMM of
+    // tile j-1), or the P^T region once PV(j-1) is done (R = 64)
+    auto gather_rope = [&](int j) {
+      if (j >= 1 && gok) {
+        if (Cfg::kRopeInP)
+          wwait(&c.p_free, (j - 1) & 1);
+        else
+          wwait(&c.rope_empty, (j - 1) & 1);
+      }
+      if (gok) gather(true, j, 0, sRope, &c.rope_full, j & 1);
     };
 
     // Softmax of tile j for this warpgroup's columns; false when the CTA
@@ -451,8 +487,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
       tc_fence_after();
       const uint32_t tS = tmem + sb * R + lane_off + cbase;
       float s[RC];
-#pragma unroll
-      for (int cc = 0; cc < RC / 16; ++cc) tmem_ld16(tS + cc * 16, s + cc * 16);
+      if (RC == 16) {
+        tmem_ld16(tS, s);
+      } else {
+        tmem_ld8(tS, s);
+      }
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&c.s_free[sb]);  // the next-but-one score GEMM may overwrite it
@@ -468,9 +507,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
         c.pf_ok[grp] = (j == 0 || mbar_wait(&c.p_free, (j - 1) & 1, abort, a.status)) ? 1 : 0;
       // the reference of a row moves only when a score passes it by more than
       // 2^8 (always on its first finite score); otherwise no row maxima
+      float m[RC];
       bool over = false;
 #pragma unroll
-      for (int r = 0; r < RC; ++r) over |= s[r] > c.m_ref[cbase + r] + 8.f;
+      for (int r = 0; r < RC; ++r) {
+        m[r] = c.m_ref[cbase + r];
+        over |= s[r] > m[r] + 8.f;
+      }
       const bool move = named_bar_or(bar_id, 128, over);
       if (!*reinterpret_cast<volatile int *>(&c.pf_ok[grp])) return false;
       if (move) {
@@ -479,7 +522,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
 #pragma unroll
           for (int r = 0; r < RC; ++r) v[r] = s[r];
           warp_transpose_reduce<RC, true>(v, lane);
-          if (RC == 32 || (lane & 1) == 0) c.red[grp][q4][RC == 32 ? lane : (lane >> 1)] = v[0];
+          if ((lane & (kSpread - 1)) == 0) c.red[grp][q4][lane / kSpread] = v[0];
         }
         named_bar_sync(bar_id, 128);
         if (t < RC) {
@@ -494,36 +537,40 @@ __global__ void __launch_bounds__(kWThreads, 1)
           if (j > 0 && m_new != m_old) c.need_rescale[grp] = j + 1;
         }
         named_bar_sync(bar_id, 128);
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+          m[r] = c.m_ref[cbase + r];
+          l_part[r] *= c.alpha[cbase + r];
+        }
       }
       const bool rescale = move && c.need_rescale[grp] == j + 1;
       uint32_t pk[RC / 2];
 #pragma unroll
       for (int r = 0; r < RC; r += 2) {
-        const float m0 = c.m_ref[cbase + r], m1 = c.m_ref[cbase + r + 1];
-        const float p0 = fast_exp2(s[r] - (m0 == -INFINITY ? 0.f : m0));
-        const float p1 = fast_exp2(s[r + 1] - (m1 == -INFINITY ? 0.f : m1));
+        const float p0 = fast_exp2(s[r] - (m[r] == -INFINITY ? 0.f : m[r]));
+        const float p1 = fast_exp2(s[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]));
         pk[r / 2] = pack_bf16x2(p0, p1);
-        if (move) {
-          l_part[r] = l_part[r] * c.alpha[cbase + r] + p0;
-          l_part[r + 1] = l_part[r + 1] * c.alpha[cbase + r + 1] + p1;
-        } else {
-          l_part[r] += p0;
-          l_part[r + 1] += p1;
-        }
+        l_part[r] += p0;
+        l_part[r + 1] += p1;
       }
       tc_fence_after();
       if (rescale) {
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-          for (int cc = 0; cc < RC / 16; ++cc) {
-            float o[16];
-            const uint32_t col = tO + lane_off + ch * R + cbase + cc * 16;
+          float o[RC];
+          const uint32_t col = tO + lane_off + ch * R + cbase;
+          if (RC == 16) {
             tmem_ld16(col, o);
-            tmem_ld_wait();
+          } else {
+            tmem_ld8(col, o);
+          }
+          tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 16; ++x) o[x] *= c.alpha[cbase + cc * 16 + x];
+          for (int x = 0; x < RC; ++x) o[x] *= c.alpha[cbase + x];
+          if (RC == 16) {
             tmem_st16(col, o);
+          } else {
+            tmem_st8(col, o);
           }
         }
         tmem_st_wait();
@@ -543,58 +590,40 @@ __global__ void __launch_bounds__(kWThreads, 1)
       return true;
     };
 
-    // The gather sequence: ring positions in order (R = 32: each tile's rope
-    // before its pair 0; R = 64: after its pair 3).  Position p reuses the
-    // slot of position p - NP, released by the PV GEMM of that tile, which
-    // needs that tile's softmax: softmaxes are taken as the sequence reaches
-    // them, so no wait can depend on work this warpgroup has not done.
-    int next_sm = 0;
-    const int total = 4 * n_tiles;
-    for (int p = 0; p < total && ok; ++p) {
-      const int j = p >> 2, pr = p & 3;
-      if (pr == 0) {
-        if (!group_wait(&c.meta_full[j & 1], (j >> 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
-                        a.status)) {
-          ok = false;
-          break;
-        }
-        if (!Cfg::kRopeInP) {
-          // the rope slot: read by the score GEMM of tile j-1 first
-          if (j >= 1 && !group_wait(&c.rope_empty, (j - 1) & 1, t, bar_id, c.bflag[grp], seq,
-                                    abort, a.status)) {
-            ok = false;
-            break;
-          }
-          gather(true, j, 0, sRope, &c.rope_full, j & 1);
-        }
-      }
-      if (p >= NP) {
-        const int q = p - NP, jq = q >> 2;
-        while (ok && next_sm <= jq) ok = softmax(next_sm++);
-        if (!ok) break;
-        if (!group_wait(&c.empty[p % NP], (q / NP) & 1, t, bar_id, c.bflag[grp], seq, abort,
-                        a.status)) {
-          ok = false;
-          break;
-        }
-      }
-      gather(false, j, pr, sRing + (p % NP) * kWSlotBytes, &c.full[p % NP], (p / NP) & 1);
-      if (Cfg::kRopeInP && pr == 3) {
-        // the rope of tile j goes to the P^T region once PV(j-1) is done
-        if (j >= 1) {
-          while (ok && next_sm <= j - 1) ok = softmax(next_sm++);
-          if (!ok) break;
-          if (!group_wait(&c.p_free, (j - 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
-                          a.status)) {
-            ok = false;
-            break;
-          }
-        }
-        gather(true, j, 0, sRope, &c.rope_full, j & 1);
+    // The sequence.  Ring position p reuses the slot of position p - NP,
+    // released by the PV GEMM of that tile, which follows that tile's
+    // softmax; so each tile's softmax comes first, then the gathers it
+    // unblocks.  R = 32 (five slots): tile j's rope and pair 0 are gathered
+    // two tiles early, between the rest of tile j-1 and the softmax of j-2.
+    //   prologue: tile 0; R = 32 also rope and pair 0 of tile 1
+    //   tile j:   softmax(j); the rest of tile j+1; R = 32: rope and pair 0
+    //             of tile j+2
+    if (n_tiles > 0) {
+      gather_meta(0);
+      if (!Cfg::kRopeInP) gather_rope(0);
+      for (int pr = 0; pr < kWPairs; ++pr) gather_pair(0, pr);
+      if (Cfg::kRopeInP) gather_rope(0);
+      if (!Cfg::kRopeInP && n_tiles > 1) {
+        gather_meta(1);
+        gather_rope(1);
+        gather_pair(1, 0);
       }
     }
-    while (ok && next_sm < n_tiles) ok = softmax(next_sm++);
-    if (!ok && lane == 0) {
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      ok = softmax(j);
+      if (!ok) break;
+      if (j + 1 < n_tiles) {
+        if (Cfg::kRopeInP) gather_meta(j + 1);
+        for (int pr = Cfg::kRopeInP ? 0 : 1; pr < kWPairs; ++pr) gather_pair(j + 1, pr);
+        if (Cfg::kRopeInP) gather_rope(j + 1);
+      }
+      if (!Cfg::kRopeInP && j + 2 < n_tiles) {
+        gather_meta(j + 2);
+        gather_rope(j + 2);
+        gather_pair(j + 2, 0);
+      }
+    }
+    if ((!ok || !gok) && lane == 0) {
       // gathers of this warp that may still be landing; a phase another warp
       // never completed gives up after the short limit
       for (int m = n_rec > kWRec ? n_rec - kWRec : 0; m < n_rec; ++m)
@@ -607,7 +636,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (ok) {
       tc_fence_after();
       warp_transpose_reduce<RC, false>(l_part, lane);
-      if (RC == 32 || (lane & 1) == 0) c.red[grp][q4][RC == 32 ? lane : (lane >> 1)] = l_part[0];
+      if ((lane & (kSpread - 1)) == 0) c.red[grp][q4][lane / kSpread] = l_part[0];
       named_bar_sync(bar_id, 128);
       if (t < RC) {
         const int r = cbase + t;
@@ -628,38 +657,38 @@ __global__ void __launch_bounds__(kWThreads, 1)
       named_bar_sync(bar_id, 128);
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-        for (int cc = 0; cc < RC / 16; ++cc) {
-          float o[16];
-          if (n_tiles > 0) {
-            tmem_ld16(tO + lane_off + ch * R + cbase + cc * 16, o);
-            tmem_ld_wait();
+        float o[RC];
+        if (n_tiles > 0) {
+          if (RC == 16) {
+            tmem_ld16(tO + lane_off + ch * R + cbase, o);
           } else {
-#pragma unroll
-            for (int x = 0; x < 16; ++x) o[x] = 0.f;
+            tmem_ld8(tO + lane_off + ch * R + cbase, o);
           }
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int r = cbase + cc * 16 + x;
-            if (r >= r_valid || !row_ok) continue;
-            if (!MERGED) {
-              a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] =
-                  o[x] * c.inv_l[r];
-            } else if (c.gtok >= 0) {
-              // merged: stage bf16 rows [head][dv] in the idle ring, stored below
-              reinterpret_cast<__nv_bfloat16 *>(sRing)[r * CPMLA_DV + ch * 128 + t] =
-                  __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
-            }
+          for (int x = 0; x < RC; ++x) o[x] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < RC; ++x) {
+          const int r = cbase + x;
+          if (r >= r_valid || !row_ok) continue;
+          if (!MERGED) {
+            a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] = o[x] * c.inv_l[r];
+          } else if (c.gtok >= 0) {
+            // merged: stage bf16 rows [head][dv] in the idle ring, stored below
+            reinterpret_cast<__nv_bfloat16 *>(sRing)[r * CPMLA_DV + ch * 128 + t] =
+                __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
           }
         }
       }
     }
     if (MERGED) {
       // the token's heads h0 .. h0 + r_valid - 1 are one contiguous span of
-      // o_out: one bulk copy of the staged rows once both warpgroups are here
-      // (both always arrive, also after an abort, which skips the copy)
+      // o_out: one bulk copy of the staged rows once every warpgroup is here
+      // (all always arrive, also after an abort, which skips the copy)
       fence_proxy_async_smem();
-      named_bar_sync(3, 256);
+      named_bar_sync(1 + kWGroups, kWSoftmaxThreads);
       if (grp == 0 && t == 0 && !*abort && c.gtok >= 0) {
         bulk_store_s2g(a.o_out + ((int64_t)c.gtok * a.H + h0) * CPMLA_DV, sRing,
                        (uint32_t)r_valid * CPMLA_DV * 2);
