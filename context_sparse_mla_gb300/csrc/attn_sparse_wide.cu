@@ -20,8 +20,8 @@
 //     the rope and first pair of tile j+2 are gathered while tile j+1 still
 //     waits for its softmax.  R = 64 (Q alone is 72 KB): four pair slots, and
 //     the rope k-block shares the region of P^T -- the rope of tile j+1 is
-//     gathered once the PV GEMM of tile j has read P^T, and the score GEMM
-//     takes the rope last.
+//     gathered once the PV GEMM of tile j has read P^T (after the gathers of
+//     pair 1), and the score GEMM takes it between pairs 1 and 2.
 //   * Gathers: TMA four-row gathers (tile::gather4, 512 B each) issued by the
 //     16 softmax warps.  One gather takes a warp ~100-200 cycles to issue, so
 //     an SM's gather rate grows with the number of issuing warps (measured:
@@ -98,8 +98,8 @@ struct WideCtrl {
   int need_rescale[kWGroups];
   int key_row[2][kTileKeys];  // KV row of each key of a tile, -1 = masked
   float red[kWGroups][4][32];
-  float m_ref[R];
-  float alpha[R];
+  alignas(16) float m_ref[R];
+  alignas(16) float alpha[R];
   float lse[R];
   float inv_l[R];
   float sfac[R];  // merged output: sink factor per head
@@ -283,6 +283,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
           mma_commit(&c.rope_empty);
         }
         for (int p = 0; p < kWPairs; ++p) {
+          if (Cfg::kRopeInP && p == 2) {
+            // the rope (gathered after pair 1, into the P^T region once the
+            // PV GEMM of the previous tile has read it) before the last pairs
+            if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int st = 0; st < 4; ++st)
+              mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_qk, 1u);
+          }
           const uint32_t pos = 4u * i + p, slot = pos % NP;
           if (!mbar_wait(&c.full[slot], (pos / NP) & 1, abort, a.status)) {
             ok = false;
@@ -300,18 +312,6 @@ __global__ void __launch_bounds__(kWThreads, 1)
           }
         }
         if (!ok) break;
-        if (Cfg::kRopeInP) {
-          // the rope last: it sits in the P^T region, free only once the PV
-          // GEMM of the previous tile has read P^T
-          if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int st = 0; st < 4; ++st)
-            mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_qk, 1u);
-        }
         mma_commit(&c.s_full[i & 1]);
       }
       if (!ok) {
@@ -479,6 +479,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
 
     // Softmax of tile j for this warpgroup's columns; false when the CTA
     // gave up.
+    auto ld_cols = [&](uint32_t col, float *v) {
+      if (RC == 16) {
+        tmem_ld16(col, v);
+      } else {
+        tmem_ld8(col, v);
+      }
+      tmem_ld_wait();
+    };
     auto softmax = [&](int j) -> bool {
       const int sb = j & 1;
       if (!group_wait(&c.s_full[sb], (j >> 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
@@ -486,20 +494,25 @@ __global__ void __launch_bounds__(kWThreads, 1)
         return false;
       tc_fence_after();
       const uint32_t tS = tmem + sb * R + lane_off + cbase;
-      float s[RC];
-      if (RC == 16) {
-        tmem_ld16(tS, s);
-      } else {
-        tmem_ld8(tS, s);
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&c.s_free[sb]);  // the next-but-one score GEMM may overwrite it
-      {
-        const bool valid = c.key_row[sb][t] >= 0;
+      // x = score * scale * log2(e) - reference (base 2), -inf for a masked
+      // key or a padding head; a reference still at -inf gives +inf
+      float x[RC];
+      ld_cols(tS, x);
+      const bool valid = c.key_row[sb][t] >= 0;
+      float m[RC];
 #pragma unroll
-        for (int r = 0; r < RC; ++r)
-          s[r] = (valid && cbase + r < r_valid) ? s[r] * a.scale_log2 : -INFINITY;
+      for (int r = 0; r < RC; r += 4) {
+        const float4 m4 = *reinterpret_cast<const float4 *>(&c.m_ref[cbase + r]);
+        m[r] = m4.x;
+        m[r + 1] = m4.y;
+        m[r + 2] = m4.z;
+        m[r + 3] = m4.w;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < RC; ++r) {
+        x[r] = (valid && cbase + r < r_valid) ? fmaf(x[r], a.scale_log2, -m[r]) : -INFINITY;
+        mx = fmaxf(mx, x[r]);
       }
       // PV(j-1) must be done before P^T is overwritten or O^T rescaled:
       // thread 0 waits, the barrier below publishes its result
@@ -507,23 +520,19 @@ __global__ void __launch_bounds__(kWThreads, 1)
         c.pf_ok[grp] = (j == 0 || mbar_wait(&c.p_free, (j - 1) & 1, abort, a.status)) ? 1 : 0;
       // the reference of a row moves only when a score passes it by more than
       // 2^8 (always on its first finite score); otherwise no row maxima
-      float m[RC];
-      bool over = false;
-#pragma unroll
-      for (int r = 0; r < RC; ++r) {
-        m[r] = c.m_ref[cbase + r];
-        over |= s[r] > m[r] + 8.f;
-      }
-      const bool move = named_bar_or(bar_id, 128, over);
+      const bool move = named_bar_or(bar_id, 128, mx > 8.f);
       if (!*reinterpret_cast<volatile int *>(&c.pf_ok[grp])) return false;
       if (move) {
-        {
-          float v[RC];
+        // the scores again, for each column's tile maximum
+        float v[RC];
+        ld_cols(tS, v);
 #pragma unroll
-          for (int r = 0; r < RC; ++r) v[r] = s[r];
-          warp_transpose_reduce<RC, true>(v, lane);
-          if ((lane & (kSpread - 1)) == 0) c.red[grp][q4][lane / kSpread] = v[0];
+        for (int r = 0; r < RC; ++r) {
+          v[r] = (valid && cbase + r < r_valid) ? v[r] * a.scale_log2 : -INFINITY;
+          x[r] = v[r];
         }
+        warp_transpose_reduce<RC, true>(x, lane);
+        if ((lane & (kSpread - 1)) == 0) c.red[grp][q4][lane / kSpread] = x[0];
         named_bar_sync(bar_id, 128);
         if (t < RC) {
           const int r = cbase + t;
@@ -539,20 +548,24 @@ __global__ void __launch_bounds__(kWThreads, 1)
         named_bar_sync(bar_id, 128);
 #pragma unroll
         for (int r = 0; r < RC; ++r) {
-          m[r] = c.m_ref[cbase + r];
+          const float mn = c.m_ref[cbase + r];
+          x[r] = v[r] - (mn == -INFINITY ? 0.f : mn);
           l_part[r] *= c.alpha[cbase + r];
         }
       }
-      const bool rescale = move && c.need_rescale[grp] == j + 1;
+      // S^T is read: the next-but-one score GEMM may overwrite it
+      tc_fence_before();
+      mbar_arrive(&c.s_free[sb]);
       uint32_t pk[RC / 2];
 #pragma unroll
       for (int r = 0; r < RC; r += 2) {
-        const float p0 = fast_exp2(s[r] - (m[r] == -INFINITY ? 0.f : m[r]));
-        const float p1 = fast_exp2(s[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]));
+        const float p0 = fast_exp2(x[r]);
+        const float p1 = fast_exp2(x[r + 1]);
         pk[r / 2] = pack_bf16x2(p0, p1);
         l_part[r] += p0;
         l_part[r + 1] += p1;
       }
+      const bool rescale = move && c.need_rescale[grp] == j + 1;
       tc_fence_after();
       if (rescale) {
 #pragma unroll 1
@@ -590,38 +603,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
       return true;
     };
 
-    // The sequence.  Ring position p reuses the slot of position p - NP,
-    // released by the PV GEMM of that tile, which follows that tile's
-    // softmax; so each tile's softmax comes first, then the gathers it
-    // unblocks.  R = 32 (five slots): tile j's rope and pair 0 are gathered
-    // two tiles early, between the rest of tile j-1 and the softmax of j-2.
-    //   prologue: tile 0; R = 32 also rope and pair 0 of tile 1
-    //   tile j:   softmax(j); the rest of tile j+1; R = 32: rope and pair 0
-    //             of tile j+2
-    if (n_tiles > 0) {
-      gather_meta(0);
-      if (!Cfg::kRopeInP) gather_rope(0);
-      for (int pr = 0; pr < kWPairs; ++pr) gather_pair(0, pr);
-      if (Cfg::kRopeInP) gather_rope(0);
-      if (!Cfg::kRopeInP && n_tiles > 1) {
-        gather_meta(1);
-        gather_rope(1);
-        gather_pair(1, 0);
-      }
-    }
+    // The sequence: tile j's gathers, then its softmax.  Ring position p
+    // reuses the slot of position p - NP, released by the PV GEMM of that
+    // tile, which follows that tile's softmax -- done one iteration earlier.
+    // R = 32 (five slots): the rope and pair 0 of tile j+1 wait for nothing
+    // and land while the PV GEMM of tile j frees the other slots.  R = 64:
+    // the rope goes after pair 1 (the PV GEMM of tile j-1 is done by then),
+    // so the score GEMM's tail only waits for pairs 2 and 3.
     for (int j = 0; j < n_tiles && ok; ++j) {
+      gather_meta(j);
+      if (!Cfg::kRopeInP) gather_rope(j);
+      for (int pr = 0; pr < kWPairs; ++pr) {
+        gather_pair(j, pr);
+        if (Cfg::kRopeInP && pr == 1) gather_rope(j);
+      }
       ok = softmax(j);
-      if (!ok) break;
-      if (j + 1 < n_tiles) {
-        if (Cfg::kRopeInP) gather_meta(j + 1);
-        for (int pr = Cfg::kRopeInP ? 0 : 1; pr < kWPairs; ++pr) gather_pair(j + 1, pr);
-        if (Cfg::kRopeInP) gather_rope(j + 1);
-      }
-      if (!Cfg::kRopeInP && j + 2 < n_tiles) {
-        gather_meta(j + 2);
-        gather_rope(j + 2);
-        gather_pair(j + 2, 0);
-      }
     }
     if ((!ok || !gok) && lane == 0) {
       // gathers of this warp that may still be landing; a phase another warp
