@@ -549,6 +549,43 @@ def main():
     status = cpmla.device_status()
     step_ms = max_over_ranks(attn_avg + merge_avg, world)
 
+    # the decode rows alone through split-KV (each row's keys in P parts, one
+    # per shard that holds a replica), for their share of the step
+    decode = None
+    n_dec = int(prob.is_decode.sum())
+    if n_dec:
+        plan_d = cpmla.plan_for(prob, device=dev, merged=True, split_decode=True)
+        o_d = torch.empty_like(o_out)
+        l_d = torch.empty_like(lse_out)
+
+        def dstep():
+            plan_d.decode(prob.q, o_d, l_d, softmax_scale=prob.scale, sink=prob.sink,
+                          idx=prob.idx, stream=stream, **kvk)
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            dstep()
+        dev_ = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(10)]
+        for i in range(10):
+            flush.fill_(float(i))
+            dev_[i][0].record(stream)
+            dstep()
+            dev_[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert cpmla.device_status() == 0
+        dec_ms = sum(e[0].elapsed_time(e[1]) for e in dev_) / 10
+        # the same rows' result in the timed step, bit for bit up to the split
+        dt = plan_d.dec["tokens"].long()
+        assert (o_d[dt].float() - o_out[dt].float()).abs().max().item() < 0.05
+        dec_keys = int(torch.clamp(prob.token_pos()[dt.cpu()].long() + 1,
+                                   max=prob.topk if prob.topk else 1 << 62).sum())
+        decode = {"tokens": n_dec, "n_split": prob.P, "ms": round(dec_ms, 4),
+                  "share_of_step": round(dec_ms / step_ms, 5),
+                  "tflops": round(dec_keys * prob.H * FLOPS_PER_KEY_HEAD / (dec_ms * 1e-3) / 1e12,
+                                  2),
+                  "how": "mla_attn_split_kv over the decode rows alone (3 launches), CUDA "
+                         "events, L2 flushed; in the timed step the owner replica of each "
+                         "decode row computes it once inside the merged launch"}
+
     # ---------------- end to end through the public API with host buffers:
     # every step partitions its batch on the host, copies its inputs and the
     # partition maps up from pinned host memory and its result back down.
@@ -694,6 +731,7 @@ def main():
                 "how": "per step: host partition, inputs + maps up from pinned memory, one "
                        "path call, O + LSE down; steps pipelined over two buffer sets and "
                        "three streams"},
+        "decode_rows": decode,
         "gpu_launches": (1 if merged else 2) * args.steps,
         "clocks": clk.summary(),
         "device_status": status,

@@ -48,6 +48,9 @@ _SIGS = {
     "pcp_ratio2_linkage_size": (_I, [_I, _I, _P, _P, _P]),
     "pcp_ratio2_linkage": (_I, [_I, _I] + [_P] * 8),
     "pcp_gather_rows_f32": (_I, [_P, _I64, _I64, _I, _I, _P, _P, _I64, _P]),
+    "mla_attn_split_kv_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
+    "mla_attn_split_kv": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I, _P,
+                               _I, _I, _F, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _lock = threading.Lock()
@@ -228,6 +231,37 @@ def mla_attn_merged(q, kv_start, rows, pos, req, owner_row, o_out, lse_out, *, s
         _check(lib().mla_attn_sparse_merged(*common, _ptr(topk_idx), topk_idx.shape[1], *tail))
 
 
+def split_kv_workspace(H, n_tokens, n_split, device="cuda"):
+    """A device buffer of the size mla_attn_split_kv needs (uint8, 256-byte
+    aligned by the caching allocator)."""
+    n = lib().mla_attn_split_kv_workspace_size(H, n_tokens, n_split)
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def mla_attn_split_kv(q, kv_start, tokens, pos, req, o_out, lse_out, *, softmax_scale, n_split,
+                      workspace, sink=None, topk_idx=None, kv=None, kv_fp8=None, kv_scale=None,
+                      kv_rope=None, stream=None):
+    """Attention of the listed tokens (int32 tokens/pos/req on the device),
+    each token's keys split into n_split parts computed side by side and
+    merged with the sink once; writes their rows of o_out [T, H, 512] bf16
+    and lse_out [T, H].  Dense causal when topk_idx is None."""
+    fmt, s_kv = _attn_common(q, kv, kv_fp8, kv_scale, kv_rope)
+    T = lse_out.shape[0]
+    k = 0
+    if topk_idx is not None:
+        _dev(topk_idx, torch.int32, "topk_idx")
+        k = topk_idx.shape[1]
+    _dev(workspace, torch.uint8, "workspace")
+    _check(lib().mla_attn_split_kv(
+        _ptr(q), q.stride(0), q.shape[1], fmt, _ptr(kv), _ptr(kv_fp8), _ptr(kv_scale),
+        _ptr(kv_rope), s_kv, _ptr(_dev(kv_start, torch.int64, "kv_start")),
+        _ptr(_dev(tokens, torch.int32, "tokens")), _ptr(_dev(pos, torch.int32, "pos")),
+        _ptr(_dev(req, torch.int32, "req")), tokens.numel(), _ptr(topk_idx), k, int(n_split),
+        float(softmax_scale), _ptr(_dev(sink, torch.float32, "sink")), T,
+        _ptr(_dev(o_out, torch.bfloat16, "o_out")), _ptr(_dev(lse_out, torch.float32, "lse_out")),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
 def mla_kv_cache_insert(kv, slot_mapping, *, cache=None, cache_fp8=None, cache_scale=None,
                         cache_rope=None, stream=None):
     """Write each token's latent KV row (kv [n, 576] bf16) to its cache row
@@ -305,7 +339,7 @@ class PcpPrefill:
     the fp32 partial buffers."""
 
     def __init__(self, P, cu_seqlens, q_start_pos, is_decode, kv_start, H, *, device="cuda",
-                 topk=0, merged=False):
+                 topk=0, merged=False, split_decode=False):
         self.merged = merged
         self.P, self.H, self.topk = P, H, topk
         part = pcp_dualchunk_partition(P, cu_seqlens, q_start_pos, is_decode)
@@ -313,7 +347,22 @@ class PcpPrefill:
         dev = torch.device(device)
         t = lambda a: torch.from_numpy(a).to(dev)
         self.rows, self.pos, self.req = t(part["rows"]), t(part["pos"]), t(part["req"])
-        self.owner_row = t(part["owner_row"])
+        owner = part["owner_row"]
+        # split_decode (merged only): the decode rows leave the merged launch
+        # (no row owns them there) and go through mla_attn_split_kv, each
+        # row's keys in P parts -- one per shard that holds a replica
+        self.split_decode = bool(split_decode and merged)
+        self.dec = None
+        if self.split_decode:
+            dec_rows = owner[np.flatnonzero(np.repeat(np.asarray(is_decode, np.uint8),
+                                                      np.diff(np.asarray(cu_seqlens))))]
+            if len(dec_rows):
+                self.dec = dict(tokens=t(part["rows"][dec_rows]), pos=t(part["pos"][dec_rows]),
+                                req=t(part["req"][dec_rows]))
+                owner = owner.copy()
+                owner[part["rows"][dec_rows]] = -1
+                self.dec_ws = split_kv_workspace(H, len(dec_rows), P, device=dev)
+        self.owner_row = t(owner)
         self.kv_start = torch.as_tensor(np.asarray(kv_start, np.int64)).to(dev)
         self.n_rows = len(part["rows"])
         self.T = len(part["owner_row"])
@@ -332,6 +381,14 @@ class PcpPrefill:
             mla_partial_attn_dense(q, self.kv_start, self.rows, self.pos, self.req, self.o_part,
                                    self.lse_part, softmax_scale=softmax_scale, stream=stream, **kv)
 
+    def decode(self, q, o_out, lse_out, *, softmax_scale, sink=None, idx=None, stream=None,
+               **kv):
+        """The decode rows through split-KV (split_decode plans only)."""
+        mla_attn_split_kv(q, self.kv_start, self.dec["tokens"], self.dec["pos"], self.dec["req"],
+                          o_out, lse_out, softmax_scale=softmax_scale, n_split=self.P,
+                          workspace=self.dec_ws, sink=sink, topk_idx=idx if self.topk else None,
+                          stream=stream, **kv)
+
     def merge(self, o_out, lse_out, sink=None, stream=None):
         lse_merge_with_sink(self.o_part, self.lse_part, self.owner_row, o_out, lse_out, sink=sink,
                             stream=stream)
@@ -346,6 +403,9 @@ class PcpPrefill:
             mla_attn_merged(q, self.kv_start, self.rows, self.pos, self.req, self.owner_row,
                             o_out, lse_out, softmax_scale=softmax_scale, sink=sink,
                             topk_idx=idx if self.topk else None, stream=stream, **kv)
+            if self.dec is not None:
+                self.decode(q, o_out, lse_out, softmax_scale=softmax_scale, sink=sink, idx=idx,
+                            stream=stream, **kv)
             return o_out, lse_out
         self.attention(q, softmax_scale=softmax_scale, idx=idx, stream=stream, **kv)
         self.merge(o_out, lse_out, sink=sink, stream=stream)
@@ -359,7 +419,7 @@ def kv_kwargs(prob):
     return dict(kv_fp8=prob.kv_fp8, kv_scale=prob.kv_scale, kv_rope=prob.kv_rope)
 
 
-def plan_for(prob, device="cuda", merged=False):
+def plan_for(prob, device="cuda", merged=False, split_decode=False):
     return PcpPrefill(prob.P, prob.cu_seqlens.numpy(), prob.q_start_pos.numpy(),
                       prob.is_decode.numpy(), prob.kv_start.numpy(), prob.H, device=device,
-                      topk=prob.topk, merged=merged)
+                      topk=prob.topk, merged=merged, split_decode=split_decode)

@@ -40,16 +40,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv_format,
                const void *kv, const void *kv_fp8, const float *kv_scale, const void *kv_rope,
                int64_t s_kv, const int64_t *kv_start, const int32_t *rows, const int32_t *pos,
                const int32_t *req, int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
                const int32_t *topk, int k, float softmax_scale, float *o_part, float *lse_part,
                const int32_t *owner_row, int T, const float *sink, void *o_out, float *lse_out,
-               void *stream) {
+               void *stream, const AttnExtra &extra) {
   const bool merged = o_out != nullptr;
-  const char *fn = merged ? (sparse ? "mla_attn_sparse_merged" : "mla_attn_dense_merged")
-                          : (sparse ? "mla_partial_attn_sparse" : "mla_partial_attn_dense");
+  const char *fn = extra.fn ? extra.fn
+                   : merged ? (sparse ? "mla_attn_sparse_merged" : "mla_attn_dense_merged")
+                            : (sparse ? "mla_partial_attn_sparse" : "mla_partial_attn_dense");
   CPMLA_CHECK_ARG(n_rows >= 0, "%s: n_rows=%d < 0", fn, n_rows);
   CPMLA_CHECK_ARG(H >= 1 && H <= 128 && (H <= 64 || H % 64 == 0),
                   "%s: H=%d unsupported (1..64, or a multiple of 64 up to 128)", fn, H);
@@ -107,6 +110,8 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   args.kv_hi = kv_hi;
   args.topk = topk;
   args.k = k;
+  args.ent_lo = extra.ent_lo;
+  args.ent_len = extra.ent_len;
   args.scale_log2 = softmax_scale * 1.4426950408889634f;
   args.o_part = o_part;
   args.lse_part = lse_part;
@@ -122,7 +127,9 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   int R;
   if (!sparse) {
     args.hc = H <= 64 ? H : 64;
-    args.g = 64 / args.hc;
+    // a work item takes g = 64 / hc consecutive shard rows over the union
+    // of their key ranges; rows that split one token's keys go one per item
+    args.g = extra.one_row_per_item ? 1 : 64 / args.hc;
     R = 64;
   } else {
     // one token per CTA.  fp8 works on 16 heads at a time (its split-P
@@ -189,7 +196,6 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   return launch_dense(args, tm, (int)n_items, st);
 }
 
-}  // namespace
 }  // namespace cpmla
 
 extern "C" int mla_partial_attn_dense(const void *q, int64_t q_token_stride, int H, int kv_format,
@@ -202,7 +208,7 @@ extern "C" int mla_partial_attn_dense(const void *q, int64_t q_token_stride, int
   return cpmla::attn_entry(false, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope,
                            s_kv, kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, nullptr, 0,
                            softmax_scale, o_part, lse_part, nullptr, 0, nullptr, nullptr,
-                           nullptr, stream);
+                           nullptr, stream, cpmla::AttnExtra{});
 }
 
 extern "C" int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, int H,
@@ -216,7 +222,7 @@ extern "C" int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, in
   return cpmla::attn_entry(true, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope,
                            s_kv, kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, topk_idx, k,
                            softmax_scale, o_part, lse_part, nullptr, 0, nullptr, nullptr,
-                           nullptr, stream);
+                           nullptr, stream, cpmla::AttnExtra{});
 }
 
 extern "C" int mla_attn_dense_merged(const void *q, int64_t q_token_stride, int H, int kv_format,
@@ -231,7 +237,7 @@ extern "C" int mla_attn_dense_merged(const void *q, int64_t q_token_stride, int 
   CPMLA_CHECK_ARG(n_rows == 0 || o_out, "mla_attn_dense_merged: o_out is NULL");
   return attn_entry(false, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope, s_kv,
                     kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, nullptr, 0, softmax_scale,
-                    nullptr, nullptr, owner_row, T, sink, o_out, lse_out, stream);
+                    nullptr, nullptr, owner_row, T, sink, o_out, lse_out, stream, AttnExtra{});
 }
 
 extern "C" int mla_attn_sparse_merged(const void *q, int64_t q_token_stride, int H, int kv_format,
@@ -246,5 +252,5 @@ extern "C" int mla_attn_sparse_merged(const void *q, int64_t q_token_stride, int
   CPMLA_CHECK_ARG(n_rows == 0 || o_out, "mla_attn_sparse_merged: o_out is NULL");
   return attn_entry(true, q, q_token_stride, H, kv_format, kv, kv_fp8, kv_scale, kv_rope, s_kv,
                     kv_start, rows, pos, req, n_rows, kv_lo, kv_hi, topk_idx, k, softmax_scale,
-                    nullptr, nullptr, owner_row, T, sink, o_out, lse_out, stream);
+                    nullptr, nullptr, owner_row, T, sink, o_out, lse_out, stream, AttnExtra{});
 }

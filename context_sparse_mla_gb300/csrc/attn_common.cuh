@@ -43,6 +43,11 @@ struct AttnArgs {
   const int32_t *kv_hi;
   const int32_t *topk;
   int k;
+  // Optional top-k window per shard row (split-KV rows): row i reads entries
+  // ent_lo[i] .. ent_lo[i] + ent_len - 1 of its token's list (clipped to k);
+  // NULL = the whole list.
+  const int32_t *ent_lo;
+  int ent_len;
   float scale_log2;  // softmax scale * log2(e)
   float *o_part;
   float *lse_part;
@@ -59,6 +64,20 @@ struct AttnArgs {
   int n_hgroups;  // H / hc
   int *status;
 };
+
+// The part of its token's top-k list a sparse shard row reads: entries
+// [e0, e0 + *len) of the row of global token g.
+__device__ __forceinline__ const int32_t *topk_window(const AttnArgs &a, int row, int64_t g,
+                                                      int *len) {
+  int e0 = 0, n = a.k;
+  if (a.ent_lo) {
+    e0 = a.ent_lo[row];
+    e0 = e0 < 0 ? 0 : (e0 > a.k ? a.k : e0);
+    n = a.k - e0 < a.ent_len ? a.k - e0 : a.ent_len;
+  }
+  *len = n;
+  return a.topk + g * a.k + e0;
+}
 
 // Sink factor of a merged row with natural-log LSE L: 1 / (1 + e^(sink - L)),
 // written as the merge kernel computes it, so that a fused epilogue and the
@@ -149,6 +168,32 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, int t
   named_bar_sync(bar_id, 128);
   return *reinterpret_cast<volatile int *>(f) != 0;
 }
+
+// Options of attn_entry beyond the public entry points' arguments.
+struct AttnExtra {
+  const int32_t *ent_lo = nullptr;  // per-row top-k window (sparse)
+  int ent_len = 0;
+  bool one_row_per_item = false;     // dense: one shard row per work item
+  const char *fn = nullptr;          // entry-point name for error messages
+};
+
+// Argument checks, work decomposition and launch of the partial-attention
+// kernels (attn.cu); the public entry points and the split-KV path call it.
+int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv_format,
+               const void *kv, const void *kv_fp8, const float *kv_scale, const void *kv_rope,
+               int64_t s_kv, const int64_t *kv_start, const int32_t *rows, const int32_t *pos,
+               const int32_t *req, int n_rows, const int32_t *kv_lo, const int32_t *kv_hi,
+               const int32_t *topk, int k, float softmax_scale, float *o_part, float *lse_part,
+               const int32_t *owner_row, int T, const float *sink, void *o_out, float *lse_out,
+               void *stream, const AttnExtra &extra);
+
+// The merge of merge.cu for a list of tokens: merged row i (partials
+// contrib_off[i] .. contrib_off[i+1]-1) is written to token out_tok[i] of
+// o_out / lse_out (T_out tokens).
+int launch_merge_to_tokens(const float *o_part, const float *lse_part, int64_t n_part, int H,
+                           const int32_t *contrib_off, const int32_t *contrib_rows, int n,
+                           const float *sink, void *o_out, float *lse_out,
+                           const int32_t *out_tok, int T_out, int *status, cudaStream_t st);
 
 // Launchers (one per translation unit); n_items CTAs, one work item each.
 int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st);

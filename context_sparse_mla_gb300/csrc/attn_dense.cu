@@ -191,6 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           record_status(a.status, CPMLA_ERR_INDEX);
         else if (a.owner_row[tok] == i)
           own = tok;
+        // a row that does not own its token (a replicated decode row outside
+        // its owner shard) computes nothing
+        if (own < 0) {
+          lo = 1;
+          hi = 0;
+          tok = -1;
+        }
       }
     }
     c.tlo[tid] = lo;

@@ -255,17 +255,7 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     for (int s = 0; s < 3; ++s) mbar_init(&c.drain[s], 1);
     c.abort = 0;
     c.need_rescale = 0;
-    // last non-empty slot of the token's top-k list
-    int last = -1;
-    if (row < a.n_rows) {
-      const int32_t *lst = a.topk + (int64_t)a.rows[row] * a.k;
-      for (int e = a.k - 1; e >= 0; --e)
-        if (lst[e] >= 0) {
-          last = e;
-          break;
-        }
-    }
-    c.n_tiles = (last + kTileKeys) / kTileKeys;
+    c.n_tiles = -1;  // the last non-empty slot of the row's list, found below
     fence_mbar_init();
   }
   if (tid == 32) {
@@ -285,10 +275,23 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
   }
+  __syncthreads();
+  // The last non-empty slot of the row's list (every thread scans its share;
+  // the loads are independent).  Merged: a row that does not own its token
+  // (a replicated decode row outside its owner shard) computes nothing.
+  if (row < a.n_rows && (!MERGED || c.gtok >= 0)) {
+    int len = 0;
+    const int32_t *lst = topk_window(a, row, a.rows[row], &len);
+    int last = -1;
+    for (int e = tid; e < len; e += NT)
+      if (__ldg(lst + e) >= 0) last = e;
+    if (last >= 0) atomicMax(&c.n_tiles, last);
+  }
   // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero padding
   // rows): the token once, then every thread's loads before its stores
   {
-    const int64_t gq = row < a.n_rows ? (int64_t)a.rows[row] : -1;
+    const int64_t gq =
+        (row < a.n_rows && (!MERGED || c.gtok >= 0)) ? (int64_t)a.rows[row] : -1;
     constexpr int kChunks = R * (CPMLA_DQK / 8);
     constexpr int kPer = (kChunks + NT - 1) / NT;
     uint4 v[kPer];
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  const int n_tiles = c.n_tiles;
+  const int n_tiles = (c.n_tiles + kTileKeys) / kTileKeys;
   const uint32_t tO = tmem + 2 * NS * R;  // O^T chunk ch at tO + ch*R; S^T buffer b at tmem + b*NS*R
   volatile int *abort = &c.abort;
 
@@ -676,16 +679,16 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
     const bool meta = warp >= kGatherWarp0;
     const int widx = meta ? (MODE == kSparseFp8 ? 0 : 2) + warp - kGatherWarp0 : warp - 2;
     const int t = tid - kGatherWarp0 * 32;  // key of a tile (meta warps)
-    int tpos = 0, lo = 0, hi = 0, p_next = -1;
+    int tpos = 0, lo = 0, hi = 0, p_next = -1, len = 0;
     int64_t base = 0;
     const int32_t *lst = nullptr;
     if (meta) {
       tpos = a.pos[row];
       base = a.kv_start[a.req[row]];
-      lst = a.topk + (int64_t)a.rows[row] * a.k;
+      lst = topk_window(a, row, a.rows[row], &len);
       lo = a.kv_lo ? a.kv_lo[row] : 0;
       hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
-      p_next = (n_tiles > 0 && t < a.k) ? lst[t] : -1;
+      p_next = (n_tiles > 0 && t < len) ? lst[t] : -1;
     }
     int seq = 0;
     bool ok = true;
@@ -701,7 +704,7 @@ __global__ void __launch_bounds__(sparse_threads<MODE>(), 1)
         const int p = p_next;
         {
           const int e = (tile + 1) * kTileKeys + t;
-          p_next = (tile + 1 < n_tiles && e < a.k) ? lst[e] : -1;
+          p_next = (tile + 1 < n_tiles && e < len) ? lst[e] : -1;
         }
         int src = -1;
         if (p >= 0) {

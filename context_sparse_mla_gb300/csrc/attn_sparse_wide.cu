@@ -206,15 +206,18 @@ __global__ void __launch_bounds__(kWThreads, 1)
     c.alpha[tid] = 1.f;
   }
   __syncthreads();
-  const bool row_ok = c.row_ok != 0;
+  // Merged: a row that does not own its token (a replicated decode row
+  // outside its owner shard) computes nothing.
+  const bool row_ok = c.row_ok != 0 && (!MERGED || c.gtok >= 0);
   const int64_t gq = row_ok ? (int64_t)a.rows[row] : -1;
   {
-    // the last non-empty slot of the token's list: every thread scans its
+    // the last non-empty slot of the row's list: every thread scans its
     // share (the loads are independent), one shared atomic each
     if (row_ok) {
-      const int32_t *lst = a.topk + gq * a.k;
+      int len = 0;
+      const int32_t *lst = topk_window(a, row, gq, &len);
       int last = -1;
-      for (int e = tid; e < a.k; e += kWThreads)
+      for (int e = tid; e < len; e += kWThreads)
         if (__ldg(lst + e) >= 0) last = e;
       if (last >= 0) atomicMax(&c.last_slot, last);
     }
@@ -364,14 +367,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
     if (row_ok && n_tiles > 0) {
       const int tpos = a.pos[row];
       const int64_t base = a.kv_start[a.req[row]];
-      const int32_t *lst = a.topk + gq * a.k;
+      int len = 0;
+      const int32_t *lst = topk_window(a, row, gq, &len);
       const int lo = a.kv_lo ? a.kv_lo[row] : 0;
       const int hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
       int nxt[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int e = q * 32 + lane;
-        nxt[q] = e < a.k ? __ldg(lst + e) : -1;
+        nxt[q] = e < len ? __ldg(lst + e) : -1;
       }
       for (int j = 0; j < n_tiles; ++j) {
         int cur[4];
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         for (int q = 0; q < 4; ++q) {
           cur[q] = nxt[q];
           const int e = (j + 1) * kTileKeys + q * 32 + lane;
-          nxt[q] = (j + 1 < n_tiles && e < a.k) ? __ldg(lst + e) : -1;
+          nxt[q] = (j + 1 < n_tiles && e < len) ? __ldg(lst + e) : -1;
         }
         // the softmax of tile j-2 (and with it every gather of that tile)
         // must be done with this buffer

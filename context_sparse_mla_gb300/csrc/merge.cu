@@ -45,7 +45,8 @@ __global__ void __launch_bounds__(kMergeThreads)
                      int64_t n_part, int H, const int32_t *__restrict__ contrib_off,
                      const int32_t *__restrict__ contrib_rows, int T,
                      const float *__restrict__ sink, __nv_bfloat16 *__restrict__ o_out,
-                     float *__restrict__ lse_out, int *status) {
+                     float *__restrict__ lse_out, const int32_t *__restrict__ out_tok,
+                     int T_out, int *status) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
   const int64_t n_warps = (int64_t)gridDim.x * (kMergeThreads / 32);
@@ -53,6 +54,15 @@ __global__ void __launch_bounds__(kMergeThreads)
   for (int64_t gh = warp; gh < total; gh += n_warps) {
     const int64_t g = gh / H;
     const int h = (int)(gh - g * H);
+    // where merged row g goes: itself, or token out_tok[g] (a list of tokens)
+    int64_t go = g;
+    if (out_tok) {
+      go = out_tok[g];
+      if (go < 0 || go >= T_out) {
+        if (lane == 0) record_status(status, CPMLA_ERR_INDEX);
+        continue;
+      }
+    }
     int c0, c1;
     if (contrib_off) {
       c0 = contrib_off[g];
@@ -109,12 +119,12 @@ __global__ void __launch_bounds__(kMergeThreads)
         for (int i = 0; i < kVecPerLane * 4; ++i) acc[i] *= f;
       }
     }
-    __nv_bfloat16 *dst = o_out + ((int64_t)g * H + h) * CPMLA_DV;
+    __nv_bfloat16 *dst = o_out + (go * H + h) * CPMLA_DV;
 #pragma unroll
     for (int i = 0; i < kVecPerLane; ++i)
       st_stream_bf16x4(dst + 4 * (lane + 32 * i), acc[4 * i], acc[4 * i + 1], acc[4 * i + 2],
                        acc[4 * i + 3]);
-    if (lane == 0) lse_out[(int64_t)g * H + h] = L;
+    if (lane == 0) lse_out[go * H + h] = L;
   }
 }
 
@@ -147,8 +157,33 @@ extern "C" int lse_merge_with_sink(const float *o_part, const float *lse_part, i
   const int grid = (int)(want < cap ? want : cap);
   lse_merge_kernel<<<grid, kMergeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       o_part, lse_part, n_part, H, contrib_off, contrib_rows, T, sink,
-      static_cast<__nv_bfloat16 *>(o_out), lse_out, status);
+      static_cast<__nv_bfloat16 *>(o_out), lse_out, nullptr, T, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "lse_merge_with_sink: launch");
   return CPMLA_OK;
 }
+
+namespace cpmla {
+// The merge for a list of tokens: merged row i (partials contrib_off[i] ..
+// contrib_off[i+1]-1) goes to token out_tok[i] of o_out / lse_out [T_out].
+int launch_merge_to_tokens(const float *o_part, const float *lse_part, int64_t n_part, int H,
+                           const int32_t *contrib_off, const int32_t *contrib_rows, int n,
+                           const float *sink, void *o_out, float *lse_out,
+                           const int32_t *out_tok, int T_out, int *status, cudaStream_t st) {
+  int dev = 0, n_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t rows = (int64_t)n * H;
+  const int64_t want = (rows + (kMergeThreads / 32) - 1) / (kMergeThreads / 32);
+  const int64_t cap = (int64_t)(n_sm > 0 ? n_sm : 152) * 8;
+  const int grid = (int)(want < cap ? want : cap);
+  if (grid <= 0) return CPMLA_OK;
+  lse_merge_kernel<<<grid, kMergeThreads, 0, st>>>(o_part, lse_part, n_part, H, contrib_off,
+                                                   contrib_rows, n, sink,
+                                                   static_cast<__nv_bfloat16 *>(o_out), lse_out,
+                                                   out_tok, T_out, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "split-KV merge: launch");
+  return CPMLA_OK;
+}
+}  // namespace cpmla

@@ -207,7 +207,8 @@ int pcp_gather_rows_f32(const float *src, int64_t src_row_stride, int64_t n_src,
  *                KV row must be finite: the sparse kernel reads row 0 in
  *                place of an empty or skipped top-k slot (weight exactly 0)
  *   kv_start     int64 [B] KV row of request b's position 0
- *   rows, pos, req  int32 [n_rows] as produced by pcp_dualchunk_partition
+ *   rows, pos, req  int32 [n_rows] as produced by pcp_dualchunk_partition;
+ *                every rows[i] must index a token of q (and of topk_idx)
  *   n_rows       shard rows to compute (host); 0 is a no-op
  *   kv_lo, kv_hi int32 [n_rows] or NULL: inclusive position range a row may use
  *   topk_idx     int32 [T, k] (sparse) request-local key positions by global
@@ -249,7 +250,9 @@ int mla_partial_attn_sparse(const void *q, int64_t q_token_stride, int H, int kv
  * with the same fp32 operations, in the same order, as the partial
  * attention followed by lse_merge_with_sink; an empty row gives O = 0,
  * LSE = -inf.  Replica rows that do not own their token (decode rows in
- * shards other than their owner) write nothing.
+ * shards other than their owner) compute and write nothing, so a replicated
+ * decode row is computed once; a caller that sets owner_row[g] = -1 leaves
+ * token g to another call (e.g. mla_attn_split_kv).
  *
  * Arguments as in section 2, without o_part / lse_part, plus (device unless
  * noted):
@@ -359,6 +362,58 @@ int mla_kv_cache_insert(const void *kv, int64_t kv_token_stride, int n,
 int mla_topk_select(const float *logits, int64_t logits_row_stride, int n_rows,
                     const int32_t *row_len, int max_row_len, int k, int32_t *topk_idx,
                     void *stream);
+
+/* --------------------------------------------------------------------------
+ * 2e. Split-KV attention of a list of tokens (device)
+ *
+ * "[Core] Add MRV2 virtual-batch PCP for MLA", "PCP algorithm": decode rows
+ * are replicated on every PCP rank; "[DeepSeekV4][PCP] ...", "Implementation
+ * summary": partial (output, LSE) pairs are merged by LSE and the sink is
+ * applied once.  A decode row (one query over a long context or top-k list)
+ * is one work item in sections 2 / 2b; here each listed token's keys are cut
+ * into n_split parts, one work item each -- as if each replica of the row took
+ * one part -- and the parts are merged with the sink once (the library's own
+ * split; the pages give none):
+ *   dense  (topk_idx == NULL): part s of a token at position t takes positions
+ *          floor((t+1) s / n_split) .. floor((t+1)(s+1) / n_split) - 1
+ *   sparse: part s takes entries s*ke .. (s+1)*ke - 1 of the token's top-k
+ *          list, ke = ceil(k / n_split)
+ * Result for token tokens[i] (natural-log LSE without the sink, as in 2b):
+ *   lse_out[tokens[i], h] = ln sum over its keys of exp(s_j)
+ *   o_out[tokens[i], h, :] = bf16( O * 1 / (1 + exp(sink[h] - LSE)) )
+ * Nothing else of o_out / lse_out is written.
+ *
+ * Arguments (device unless noted): q, q_token_stride, H, kv_format, kv,
+ * kv_fp8, kv_scale, kv_rope, s_kv, kv_start, softmax_scale as in section 2;
+ *   tokens, pos, req  int32 [n_tokens]: global token, position in its request
+ *                and request index of each listed token (e.g. the decode rows
+ *                of a batch, pos = context length - 1)
+ *   n_tokens     (host) >= 0; 0 is a no-op
+ *   topk_idx, k  as in section 2 (indexed by global token), or NULL / 0 for
+ *                dense causal attention
+ *   n_split      (host) 1..64
+ *   sink         fp32 [H] or NULL; T (host) tokens of o_out / lse_out
+ *   o_out        bf16 [T, H, 512], lse_out fp32 [T, H] outputs (16-byte
+ *                aligned); a token outside [0, T) is skipped and recorded as
+ *                CPMLA_ERR_INDEX in the status word
+ *   workspace    device scratch of at least
+ *                mla_attn_split_kv_workspace_size(H, n_tokens, n_split) bytes,
+ *                256-byte aligned, owned by the caller; it holds the parts'
+ *                row arrays and their fp32 partial O and LSE (about 2 KB per
+ *                part and head), and must not be in use by other work until
+ *                this call's work on `stream` is done
+ * Errors: CPMLA_ERR_ARG (incl. a workspace that is too small or misaligned),
+ * CPMLA_ERR_UNSUPPORTED, CPMLA_ERR_CUDA.  Three launches on `stream`.
+ * mla_attn_split_kv_workspace_size returns 0 for invalid sizes.
+ * ------------------------------------------------------------------------ */
+size_t mla_attn_split_kv_workspace_size(int H, int n_tokens, int n_split);
+
+int mla_attn_split_kv(const void *q, int64_t q_token_stride, int H, int kv_format, const void *kv,
+                      const void *kv_fp8, const float *kv_scale, const void *kv_rope, int64_t s_kv,
+                      const int64_t *kv_start, const int32_t *tokens, const int32_t *pos,
+                      const int32_t *req, int n_tokens, const int32_t *topk_idx, int k,
+                      int n_split, float softmax_scale, const float *sink, int T, void *o_out,
+                      float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /* --------------------------------------------------------------------------
  * 3. Global LSE merge + attention sink once + restore to global order (device)

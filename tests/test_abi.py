@@ -165,3 +165,23 @@ def test_merge_argument_checks(lib):
 def test_selftest_limit_checked_before_the_device(lib):
     assert lib.cpmla_selftest_wait_timeout(0, None) == cpmla.CPMLA_ERR_ARG
     assert lib.cpmla_selftest_wait_timeout(5000, None) == cpmla.CPMLA_ERR_ARG
+
+
+def test_split_kv_argument_checks(lib):
+    size = lib.mla_attn_split_kv_workspace_size
+    assert size(64, 32, 8) >= 32 * 8 * 64 * (512 * 4 + 4)
+    assert size(64, 32, 8) < size(64, 32, 9) and size(0, 1, 1) == 0 and size(4, 1, 0) == 0
+    f = lib.mla_attn_split_kv
+    base = [None, 576 * 4, 4, 0, None, None, None, None, 16, None]
+    # empty is a no-op; n_split outside 1..64; a missing or short workspace
+    assert f(*base, None, None, None, 0, None, 0, 4, 0.07, None, 1, None, None, None, 0,
+             None) == cpmla.CPMLA_OK
+    assert f(*base, None, None, None, 1, None, 0, 0, 0.07, None, 1, None, None, None, 0,
+             None) == cpmla.CPMLA_ERR_ARG
+    assert f(*base, None, None, None, 1, None, 0, 65, 0.07, None, 1, None, None, None, 0,
+             None) == cpmla.CPMLA_ERR_ARG
+    buf = ctypes.create_string_buffer(1 << 12)
+    addr = (ctypes.addressof(buf) + 255) & ~255
+    assert f(*base, 8, 8, 8, 1, None, 0, 2, 0.07, None, 1, 8, 8, addr, 16,
+             None) == cpmla.CPMLA_ERR_ARG
+    assert b"workspace" in lib.cpmla_last_error()
