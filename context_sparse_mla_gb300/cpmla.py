@@ -51,6 +51,8 @@ _SIGS = {
     "mla_attn_split_kv_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "mla_attn_split_kv": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _I, _P,
                                _I, _I, _F, _P, _I, _P, _P, _P, ctypes.c_size_t, _P]),
+    "mla_attn_split_kv_noalloc": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _I64, _P, _P, _P, _P,
+                                       _I, _P, _I, _I, _F, _P, _I, _P, _P, _P]),
 }
 
 _lock = threading.Lock()

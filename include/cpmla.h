@@ -416,6 +416,39 @@ int mla_attn_split_kv(const void *q, int64_t q_token_stride, int H, int kv_forma
                       float *lse_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /* --------------------------------------------------------------------------
+ * 2f. Split-KV attention without a caller workspace (device)
+ *
+ * No counterpart on the pages: a convenience of this library.  The same
+ * computation, arguments, results and errors as mla_attn_split_kv (2e),
+ * without workspace / workspace_bytes: the parts' partial results go to a
+ * fixed array of the library's own device memory, so the call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).  It is for
+ * callers that cannot allocate device scratch -- code hosted inside a
+ * framework that owns all device memory and gives it only inputs and
+ * outputs, or a serving loop whose memory is fixed at start-up.
+ *   - The array holds CPMLA_SPLIT_KV_STATIC_BYTES on every GPU that loads the
+ *     library, until the process exits.  A call needing more scratch than
+ *     that, mla_attn_split_kv_workspace_size(H, n_tokens, n_split) bytes,
+ *     fails with CPMLA_ERR_ARG and says so (fewer tokens or parts per call,
+ *     or use mla_attn_split_kv).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current); make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the array, which keeps the last call's
+ *     contents; nothing in it has to start at zero, but calls whose work can
+ *     overlap on the GPU (other streams, other host threads) race on it --
+ *     order them on one stream.
+ * ------------------------------------------------------------------------ */
+#define CPMLA_SPLIT_KV_STATIC_BYTES (32u << 20)
+int mla_attn_split_kv_noalloc(const void *q, int64_t q_token_stride, int H, int kv_format,
+                              const void *kv, const void *kv_fp8, const float *kv_scale,
+                              const void *kv_rope, int64_t s_kv, const int64_t *kv_start,
+                              const int32_t *tokens, const int32_t *pos, const int32_t *req,
+                              int n_tokens, const int32_t *topk_idx, int k, int n_split,
+                              float softmax_scale, const float *sink, int T, void *o_out,
+                              float *lse_out, void *stream);
+
+/* --------------------------------------------------------------------------
  * 3. Global LSE merge + attention sink once + restore to global order (device)
  *
  * "[DeepSeekV4][PCP] ...", "Implementation summary" (merge LSE/output
