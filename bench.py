@@ -38,7 +38,10 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
 NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
-                     ("topk_s8k_k2048", "topk"): 126_344_192 + 8_175_360}
+                     ("topk_s8k_k2048", "topk"): 126_344_192 + 8_175_360,
+                     # 16002-token capture of the same shape (1.432 + 1.018 GB),
+                     # scaled to the workload's 326209 tokens
+                     ("varlen_p8_h64", "merged"): int(2.450296e9 * 326209 / 16002)}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
@@ -720,7 +723,9 @@ def main():
                      "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16"], 4),
                      "traffic": NCU_TRAFFIC_BYTES.get((args.workload, args.path)),
-                     "kernel": "mla_sparse_kernel" if prob.topk else "mla_dense_kernel",
+                     "kernel": ("mla_dense_kernel" if not prob.topk else
+                                "mla_sparse_kernel" if prob.kv_format == "fp8" or prob.H <= 16
+                                else "mla_sparse_wide_kernel"),
                      "peak_source": pk["source"] + " burst bf16"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm"],
                            "unit": "GB/s", "frac": round(merge_gbs / pk["hbm"], 4),

@@ -14,6 +14,7 @@ Workloads (``WORKLOADS``):
   sparse_s128k_h16_p2_fp8  131072 tokens, 16 heads, P=2, top-2048, fp8 latent
   varlen_p8_h64         8 prefills of U[1024,65536] tokens + 32 decode rows
                         over contexts U[4096,131072], 64 heads, P=8, top-2048
+  varlen_p8_h64_s16k, sparse_s12k_h32_p4   smaller cases of the same shapes
 All values bf16 ~N(0,1); sink ~N(0,1) fp32 per head; softmax scale 1/sqrt(192).
 """
 from __future__ import annotations
@@ -213,6 +214,11 @@ WORKLOADS = {
     "sparse_s128k_h16_p2_fp8": dict(S=131072, H=16, P=2, topk=2048, kv_format="fp8"),
     "varlen_p8_h64": dict(varlen=True, n_prefill=8, len_lo=1024, len_hi=65536, n_decode=32,
                           ctx_lo=4096, ctx_hi=131072, H=64, P=8, topk=2048, kv_format="bf16"),
+    # smaller cases of the same kernels, for profiler captures (inputs larger
+    # than L2: 1.2 GB of Q, 168 MB of KV; 3.8 GB of Q, 38 MB of KV)
+    "varlen_p8_h64_s16k": dict(varlen=True, prefill_lens=[9000, 7000], decode_ctx=[40000, 90000],
+                               H=64, P=8, topk=2048, kv_format="bf16"),
+    "sparse_s12k_h32_p4": dict(S=12288, H=32, P=4, topk=2048, kv_format="bf16"),
 }
 
 
