@@ -41,7 +41,9 @@ NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
                      ("topk_s8k_k2048", "topk"): 126_344_192 + 8_175_360,
                      # 16002-token capture of the same shape (1.432 + 1.018 GB),
                      # scaled to the workload's 326209 tokens
-                     ("varlen_p8_h64", "merged"): int(2.450296e9 * 326209 / 16002)}
+                     ("varlen_p8_h64", "merged"): int(2.450296e9 * 326209 / 16002),
+                     # 12288-token capture (586.2 + 375.6 MB), scaled to 32768 tokens
+                     ("sparse_s32k_h32_p4", "merged"): int(961.832448e6 * 32768 / 12288)}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
