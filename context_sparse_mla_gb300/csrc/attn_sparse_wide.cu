@@ -669,31 +669,34 @@ __global__ void __launch_bounds__(kWThreads, 1)
 #pragma unroll
           for (int x = 0; x < RC; ++x) o[x] = 0.f;
         }
+        if (!MERGED) {
 #pragma unroll
-        for (int x = 0; x < RC; ++x) {
-          const int r = cbase + x;
-          if (r >= r_valid || !row_ok) continue;
-          if (!MERGED) {
+          for (int x = 0; x < RC; ++x) {
+            const int r = cbase + x;
+            if (r >= r_valid || !row_ok) continue;
             a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] = o[x] * c.inv_l[r];
-          } else if (c.gtok >= 0) {
-            // merged: stage bf16 rows [head][dv] in the idle ring, stored below
-            reinterpret_cast<__nv_bfloat16 *>(sRing)[r * CPMLA_DV + ch * 128 + t] =
-                __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
+          }
+        } else {
+          // merged: bf16 pairs of neighbouring dv -- lane pairs trade one
+          // value so that the even lane stores head r at dv t, t+1 and the
+          // odd lane head r+1 at dv t-1, t (4-byte stores; a warp writes two
+          // 64-byte spans per instruction)
+          const bool odd = (lane & 1) != 0;
+          const bool own = row_ok && c.gtok >= 0;
+#pragma unroll
+          for (int x = 0; x < RC; x += 2) {
+            const int r = cbase + x;
+            const float v0 = r < r_valid ? (o[x] * c.inv_l[r]) * c.sfac[r] : 0.f;
+            const float v1 = r + 1 < r_valid ? (o[x + 1] * c.inv_l[r + 1]) * c.sfac[r + 1] : 0.f;
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+            const int hr = odd ? r + 1 : r;
+            if (own && hr < r_valid) {
+              const uint32_t w = odd ? pack_bf16x2(got, v1) : pack_bf16x2(v0, got);
+              *reinterpret_cast<uint32_t *>(a.o_out + ((int64_t)c.gtok * a.H + h0 + hr) * CPMLA_DV +
+                                            ch * 128 + (t & ~1)) = w;
+            }
           }
         }
-      }
-    }
-    if (MERGED) {
-      // the token's heads h0 .. h0 + r_valid - 1 are one contiguous span of
-      // o_out: one bulk copy of the staged rows once every warpgroup is here
-      // (all always arrive, also after an abort, which skips the copy)
-      fence_proxy_async_smem();
-      named_bar_sync(1 + kWGroups, kWSoftmaxThreads);
-      if (grp == 0 && t == 0 && !*abort && c.gtok >= 0) {
-        bulk_store_s2g(a.o_out + ((int64_t)c.gtok * a.H + h0) * CPMLA_DV, sRing,
-                       (uint32_t)r_valid * CPMLA_DV * 2);
-        bulk_commit();
-        bulk_wait_read();
       }
     }
   }
