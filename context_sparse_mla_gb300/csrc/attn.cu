@@ -183,8 +183,26 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
     }
     if (cr2 != CUDA_SUCCESS)
       return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr2);
-    if (kv_format == CPMLA_KV_BF16 && R > 16)
-      return launch_sparse_wide(R, args, tm_kv, (int)n_items, st);
+    if (kv_format == CPMLA_KV_BF16 && R > 16) {
+      // Q as [T tokens, H heads, 576] with the token stride; one box is the
+      // 64 dims of one k-block for R consecutive heads of one token, in the
+      // MMA's 128-byte-swizzled K-major layout (heads past H read as zero)
+      CUtensorMap tm_q;
+      memset(&tm_q, 0, sizeof tm_q);
+      const int64_t T_q = (int64_t)(merged ? T : 0);
+      cuuint64_t qdims[3] = {(cuuint64_t)CPMLA_DQK, (cuuint64_t)H,
+                             (cuuint64_t)(T_q > 0 ? T_q : INT32_MAX)};
+      cuuint64_t qstr[2] = {(cuuint64_t)CPMLA_DQK * 2, (cuuint64_t)q_token_stride * 2};
+      cuuint32_t qbox[3] = {(cuuint32_t)kKbDims, (cuuint32_t)R, 1};
+      cuuint32_t qes[3] = {1, 1, 1};
+      const CUresult cq = enc(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q),
+                              qdims, qstr, qbox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (cq != CUDA_SUCCESS)
+        return fail(CPMLA_ERR_CUDA, "%s: Q tensor map encode failed (%d)", fn, (int)cq);
+      return launch_sparse_wide(R, args, tm_kv, tm_q, (int)n_items, st);
+    }
     return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args, tm_kv,
                          tm_rope, (int)n_items, st);
   }

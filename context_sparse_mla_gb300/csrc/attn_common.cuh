@@ -203,8 +203,9 @@ int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cu
 int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
                   const CUtensorMap &tm_rope, int n_items, cudaStream_t st);
 // Sparse, bf16 KV, R = 32 or 64 heads per CTA (attn_sparse_wide.cu); tm_kv as
-// for the bf16 narrow kernel.
-int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
-                       cudaStream_t st);
+// for the bf16 narrow kernel; tm_q: Q as [T, H, 576] in boxes of 64 dims x R
+// heads x 1 token, 128-byte swizzle.
+int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv,
+                       const CUtensorMap &tm_q, int n_items, cudaStream_t st);
 
 }  // namespace cpmla

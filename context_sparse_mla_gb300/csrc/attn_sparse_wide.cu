@@ -88,6 +88,8 @@ struct WideCtrl {
   uint64_t drain[3];      // per MMA-issuing thread
   uint64_t meta_full[2];  // key rows of a tile written: the meta warp's 32 lanes
   uint64_t meta_empty[2]; // key rows of a tile no longer needed: every softmax thread
+  uint64_t q_full;        // the token's Q rows landed (TMA)
+  uint64_t pv_c0;         // PV issuer 0 has issued dv chunk 0 of a tile
   uint32_t tmem_base;
   int abort;
   int last_slot;          // setup: the largest non-empty top-k slot of the row
@@ -134,7 +136,8 @@ __device__ __forceinline__ void wide_drain_wait(uint64_t *bar, uint32_t parity,
 template <int R, bool MERGED>
 __global__ void __launch_bounds__(kWThreads, 1)
     mla_sparse_wide_kernel(const __grid_constant__ AttnArgs a,
-                           const __grid_constant__ CUtensorMap tm_kv) {
+                           const __grid_constant__ CUtensorMap tm_kv,
+                           const __grid_constant__ CUtensorMap tm_q) {
   using Cfg = WideCfg<R>;
   constexpr int RC = Cfg::RC;
   constexpr int NP = wide_slots<R>();
@@ -165,6 +168,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       mbar_init(&c.empty[s], 1);
     }
     mbar_init(&c.rope_full, kWGatherWarps);
+    mbar_init(&c.q_full, 1);
+    mbar_init(&c.pv_c0, 1);
     mbar_init(&c.rope_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&c.s_full[s], 1);
@@ -201,6 +206,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, Cfg::kTmemCols);
   if (warp == kWGroup0 && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (warp == 1 && lane == 0) tma_prefetch_desc(&tm_q);
   if (tid < R) {
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
@@ -210,6 +216,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
   // outside its owner shard) computes nothing.
   const bool row_ok = c.row_ok != 0 && (!MERGED || c.gtok >= 0);
   const int64_t gq = row_ok ? (int64_t)a.rows[row] : -1;
+  // Q rows of this item: nine TMA boxes [R heads x 64 dims] straight into the
+  // MMA's K-major, 128-byte-swizzled k-blocks (heads past H read as zero);
+  // they land while the list is scanned and the first keys are gathered
+  if (tid == 0 && row_ok) {
+    mbar_arrive_expect_tx(&c.q_full, (uint32_t)(kKb * R * 128));
+#pragma unroll 1
+    for (int kb = 0; kb < kKb; ++kb)
+      tma_load_3d(sQ + kb * (R * 128), &tm_q, kb * kKbDims, h0, (int)gq, &c.q_full);
+  }
   {
     // the last non-empty slot of the row's list: every thread scans its
     // share (the loads are independent), one shared atomic each
@@ -221,33 +236,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         if (__ldg(lst + e) >= 0) last = e;
       if (last >= 0) atomicMax(&c.last_slot, last);
     }
-    // Q rows of this item -> K-major, 128-byte-swizzled k-blocks (zero
-    // padding rows), every thread's loads before its stores
-    constexpr int kChunks = R * (CPMLA_DQK / 8);
-    constexpr int kPer = (kChunks + kWThreads - 1) / kWThreads;
-    uint4 v[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = tid + k * kWThreads;
-      const int r = idx / (CPMLA_DQK / 8);
-      const int ch = idx - r * (CPMLA_DQK / 8);
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (idx < kChunks && r < r_valid && gq >= 0)
-        v[k] = __ldg(reinterpret_cast<const uint4 *>(a.q + gq * a.q_stride +
-                                                     (int64_t)(h0 + r) * CPMLA_DQK) +
-                     ch);
-    }
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int idx = tid + k * kWThreads;
-      if (idx >= kChunks) continue;
-      const int r = idx / (CPMLA_DQK / 8);
-      const int ch = idx - r * (CPMLA_DQK / 8);
-      const int kb = ch >> 3, cc = ch & 7;
-      *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = v[k];
-    }
   }
-  fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -265,7 +254,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
       const uint64_t drope = smem_desc(smem_u32(sRope), 16, 1024, kSwz128);
       const uint64_t dq_rope = dq0 + ((kLatKb * (R * 128)) >> 4);
-      bool ok = true;
+      bool ok = n_tiles == 0 || mbar_wait(&c.q_full, 0, abort, a.status);
       for (int i = 0; i < n_tiles && ok; ++i) {
         const uint32_t dS = tmem + (i & 1) * R;
         if (i >= 2 && !mbar_wait(&c.s_free[i & 1], ((i >> 1) - 1) & 1, abort, a.status)) {
@@ -321,6 +310,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
         mma_commit(&c.drain[0]);
         wide_drain_wait(&c.drain[0], 0, kWaitLimitNs);
       }
+      // the Q copy this thread issued has landed before the CTA can exit
+      if (row_ok) wide_drain_wait(&c.q_full, 0, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 1 || warp == 2) {
@@ -340,6 +331,12 @@ __global__ void __launch_bounds__(kWThreads, 1)
           break;
         }
         tc_fence_after();
+        // chunk 0 reaches the tensor core before the other issuer's first
+        // chunk, so the first ring slot of the tile is freed soonest
+        if (me == 1 && !mbar_wait(&c.pv_c0, j & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
         for (int ch = me; ch < kWPairs; ch += 2) {
           const uint32_t slot = (4u * j + ch) % NP;
           const uint64_t da = dr0 + ((slot * kWSlotBytes) >> 4);
@@ -349,6 +346,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                         dp0 + ((st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
                         (j > 0 || st > 0) ? 1u : 0u);
           mma_commit(&c.empty[slot]);
+          if (ch == 0) mbar_arrive(&c.pv_c0);
         }
         mma_commit(&c.p_free);
       }
@@ -711,14 +709,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
 }
 
 template <int R, bool MERGED>
-int launch_wide_t(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
-                  cudaStream_t stream) {
+int launch_wide_t(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &tm_q,
+                  int n_items, cudaStream_t stream) {
   constexpr int smem = wide_smem_bytes<R>();
   static_assert(smem <= 232448, "shared memory budget");
   auto kern = mla_sparse_wide_kernel<R, MERGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: set shared memory size");
-  kern<<<n_items, kWThreads, smem, stream>>>(args, tm_kv);
+  kern<<<n_items, kWThreads, smem, stream>>>(args, tm_kv, tm_q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: launch");
   return CPMLA_OK;
@@ -726,13 +724,13 @@ int launch_wide_t(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
 
 }  // namespace
 
-int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv, int n_items,
-                       cudaStream_t st) {
+int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv,
+                       const CUtensorMap &tm_q, int n_items, cudaStream_t st) {
   if (args.o_out)
-    return R == 64 ? launch_wide_t<64, true>(args, tm_kv, n_items, st)
-                   : launch_wide_t<32, true>(args, tm_kv, n_items, st);
-  return R == 64 ? launch_wide_t<64, false>(args, tm_kv, n_items, st)
-                 : launch_wide_t<32, false>(args, tm_kv, n_items, st);
+    return R == 64 ? launch_wide_t<64, true>(args, tm_kv, tm_q, n_items, st)
+                   : launch_wide_t<32, true>(args, tm_kv, tm_q, n_items, st);
+  return R == 64 ? launch_wide_t<64, false>(args, tm_kv, tm_q, n_items, st)
+                 : launch_wide_t<32, false>(args, tm_kv, tm_q, n_items, st);
 }
 
 }  // namespace cpmla

@@ -127,6 +127,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, in
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// TMA (tiled, 3D) global -> shared, completion on an mbarrier
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, int x, int y, int z,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 // TMA gather of four rows (r0..r3) of a 2D tensor, box = one row of the
 // tensor map's box width starting at column x; the rows land contiguously.
 __device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *tm, int x, int r0, int r1,
