@@ -132,10 +132,11 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
     args.g = extra.one_row_per_item ? 1 : 64 / args.hc;
     R = 64;
   } else {
-    // one token per CTA.  fp8 works on 16 heads at a time (its split-P
-    // region is sized for R = 16); bf16 takes up to 16 heads in the narrow
-    // kernel, up to 32 or 64 in the wide one (all heads of a 64-head token in
-    // one CTA, so its keys are gathered once)
+    // one token per CTA.  fp8 works on 16 heads at a time (its four P^T
+    // matrices and five score accumulators are sized for R = 16); bf16 takes
+    // up to 16 heads in the narrow kernel, up to 32 or 64 in the wide one
+    // (all heads of a 64-head token in one CTA, so its keys are gathered
+    // once)
     const int hmax = kv_format == CPMLA_KV_FP8_E4M3_G128 ? 16 : 64;
     args.hc = H <= hmax ? H : hmax;
     if (H > hmax && H % hmax != 0)
@@ -201,10 +202,11 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (cq != CUDA_SUCCESS)
         return fail(CPMLA_ERR_CUDA, "%s: Q tensor map encode failed (%d)", fn, (int)cq);
-      return launch_sparse_wide(R, args, tm_kv, tm_q, (int)n_items, st);
+      return launch_sparse_wide(false, R, args, tm_kv, tm_q, tm_rope, (int)n_items, st);
     }
-    return launch_sparse(kv_format == CPMLA_KV_BF16 ? kSparseBf16 : kSparseFp8, R, args, tm_kv,
-                         tm_rope, (int)n_items, st);
+    if (kv_format == CPMLA_KV_FP8_E4M3_G128)
+      return launch_sparse_wide(true, 16, args, tm_kv, tm_kv, tm_rope, (int)n_items, st);
+    return launch_sparse(kSparseBf16, R, args, tm_kv, tm_rope, (int)n_items, st);
   }
   // 128-key x 64-dim tiles of the bf16 KV
   CUtensorMap tm;

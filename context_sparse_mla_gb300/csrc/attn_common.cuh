@@ -202,10 +202,12 @@ int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cu
 // tm_rope = the bf16 rope (box 64 x 1, 128-byte swizzle).
 int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
                   const CUtensorMap &tm_rope, int n_items, cudaStream_t st);
-// Sparse, bf16 KV, R = 32 or 64 heads per CTA (attn_sparse_wide.cu); tm_kv as
-// for the bf16 narrow kernel; tm_q: Q as [T, H, 576] in boxes of 64 dims x R
-// heads x 1 token, 128-byte swizzle.
-int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv,
-                       const CUtensorMap &tm_q, int n_items, cudaStream_t st);
+// Sparse with 16 gather warps (attn_sparse_wide.cu): bf16 KV with R = 32 or
+// 64 heads per CTA, or fp8 KV with R = 16.  tm_kv and tm_rope as for
+// launch_sparse; bf16: tm_q = Q as [T, H, 576] in boxes of 64 dims x R heads
+// x 1 token, 128-byte swizzle (fp8 reads Q with plain loads; tm_q unused).
+int launch_sparse_wide(bool fp8, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
+                       const CUtensorMap &tm_q, const CUtensorMap &tm_rope, int n_items,
+                       cudaStream_t st);
 
 }  // namespace cpmla

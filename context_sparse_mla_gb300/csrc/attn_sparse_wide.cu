@@ -1,15 +1,19 @@
 // attn_sparse_wide.cu -- top-k sparse partial MLA attention (output + LSE, no
-// sink) over a bf16 latent KV for 17 to 64 heads of one token per CTA, on
-// sm_103a.
+// sink) for one token per CTA, on sm_103a: a bf16 latent KV for 17 to 64
+// heads, or the fp8 KV cache (E4M3 latent with one scale per 128 channels,
+// bf16 rope) for 16 heads at a time.
 //
 // "[DeepSeekV4][PCP] Enable context-parallel prefill for hybrid KV and
 // MegaMoE", "Implementation summary": each shard computes the partial
 // attention of its query rows over their own top-k keys, merged later by LSE
-// (or, for a token's single owner row, in this kernel's epilogue).
+// (or, for a token's single owner row, in this kernel's epilogue);
+// "[Feature][PCP] Add DeepSeek-V4.1-Flash support", "Supported Scope": the
+// sparse MLA path with an fp8 KV cache.
 //
-// One CTA = one token x R heads (R = 32 or 64).  A token's keys are its own,
-// so every gathered key row feeds only this token's heads: with R = 64 one
-// CTA covers all heads of a 64-head token and each key row is gathered once.
+// One CTA = one token x R heads (bf16: R = 32 or 64; fp8: R = 16).  A token's
+// keys are its own, so every gathered key row feeds only this token's heads:
+// with R = 64 one CTA covers all heads of a 64-head token and each key row is
+// gathered once.
 //   * Score GEMM key-major: S^T = K . Q^T, M = 128 keys, N = R, K = 576, into
 //     one of two TMEM buffers.  PV GEMM: O^T += V^T . P^T, M = 128 dv x 4
 //     chunks, N = R, K = 128 keys, V read from the k-blocks the score GEMM
@@ -39,6 +43,19 @@
 //     chunk).  Base 2, with a row reference moved only when a score passes it
 //     by 2^8.  Per tile the warps run the softmax first, then the gathers it
 //     unblocks.
+//   * fp8 (R = 16, five pair slots, a rope slot of its own): gather warp w
+//     fetches the raw E4M3 codes of keys 8 w .. 8 w + 7 of a pair (128 bytes a
+//     key, unswizzled, into the upper half of the slot) and, once they have
+//     landed, converts them in place to the two fp16 k-blocks of those keys --
+//     exactly, since every E4M3 value is an fp16 value.  The score GEMM keeps
+//     one accumulator per 128-channel scale group and one for the bf16 rope
+//     (five per S^T buffer); Q's latent part is fp16 to meet the fp16 codes.
+//     The softmax forms s = rope + sum_g scale_g x group_g, and writes one
+//     P^T per dv chunk in fp16 with that chunk's scale folded in, so the PV
+//     GEMM also runs on the exact codes.  The five accumulators are
+//     independent, so a second thread (warp 20) issues the MMAs of pairs 2
+//     and 3 beside warp 0, and each dv chunk of the PV GEMM has its own
+//     issuer (warps 1, 2, 21, 22), so a tile's slots free together.
 //   * Every wait is bounded.  A wait that decides a warpgroup's control flow
 //     is taken by one thread and published to the group, so the group's named
 //     barriers always match; a gather warp whose own wait gives up stops
@@ -61,34 +78,42 @@ constexpr int kWSlotBytes = 2 * kKbBytes;  // 32 KB pair slot
 constexpr int kWPairs = 4;                 // latent k-block pairs per tile
 constexpr int kWRec = 6;                   // gathers remembered per warp for the drain
 
-template <int R>
+template <bool FP8, int R>
 struct WideCfg {
-  static_assert(R == 32 || R == 64, "32 or 64 heads per CTA");
+  static_assert(FP8 ? R == 16 : (R == 32 || R == 64), "bf16: 32 or 64 heads per CTA; fp8: 16");
   static constexpr int RC = R / kWGroups;            // score columns per softmax warpgroup
-  static constexpr bool kRopeInP = R == 64;          // rope shares the P^T region
-  static constexpr int kPBytes = kTileKeys * R * 2;  // P^T [128 keys x R]
-  static constexpr int kPRegion = kRopeInP ? kKbBytes : kPBytes;
+  static constexpr int NS = FP8 ? 5 : 1;             // score accumulators per S^T buffer
+  static constexpr bool kRopeInP = !FP8 && R == 64;  // rope shares the P^T region
+  static constexpr int kPBytes = kTileKeys * R * 2;  // one P^T [128 keys x R]
+  // fp8: one P^T per dv chunk
+  static constexpr int kPRegion = FP8 ? 4 * kPBytes : (kRopeInP ? kKbBytes : kPBytes);
   static constexpr int kRopeSlot = kRopeInP ? 0 : kKbBytes;
   static constexpr int kQBytes = R * CPMLA_DQK * 2;
-  static constexpr uint32_t kTmemCols = 2 * R + 4 * R <= 256 ? 256 : 512;
+  static constexpr int kPvIssuers = FP8 ? 4 : 2;
+  // fp8: warp 20 (second score issuer), warps 21-22 (PV issuers 2-3)
+  static constexpr int kThreads = FP8 ? kWThreads + 96 : kWThreads;
+  static constexpr uint32_t kTmemCols = 2 * NS * R + 4 * R <= 256 ? 256 : 512;
 };
-static_assert(WideCfg<64>::kPBytes == kKbBytes, "rope k-block and P^T have one size");
+static_assert(WideCfg<false, 64>::kPBytes == kKbBytes, "rope k-block and P^T have one size");
+constexpr int kWScore2Warp = 20;  // fp8: second score-GEMM issuer (pairs 2 and 3)
+constexpr int kWPv2Warp = 21;     // fp8: PV issuers 2 and 3 (warps 21, 22)
 
-template <int R>
+template <bool FP8, int R>
 struct WideCtrl {
-  uint64_t full[8];       // pair slot landed: one arrival per gather warp
+  uint64_t full[8];       // pair slot ready for the tensor core: one arrival per gather warp
   uint64_t empty[8];      // pair slot released by its PV GEMM chunk
+  uint64_t raw[FP8 ? kWGatherWarps : 1][8];  // fp8: a gather warp's codes of a pair slot landed
   uint64_t rope_full;     // rope landed: one arrival per gather warp
   uint64_t rope_empty;    // separate rope slot read by the score GEMM
-  uint64_t s_full[2];
+  uint64_t s_full[2];     // one commit per score issuer
   uint64_t s_free[2];     // S^T buffer read: every softmax thread
   uint64_t p_full;        // P^T written: every softmax thread
-  uint64_t p_free;        // PV GEMM of a tile done: both PV issuers
-  uint64_t o_full;        // all PV GEMMs done: both PV issuers
-  uint64_t drain[3];      // per MMA-issuing thread
+  uint64_t p_free;        // PV GEMM of a tile done: every PV issuer
+  uint64_t o_full;        // all PV GEMMs done: every PV issuer
+  uint64_t drain[8];      // per MMA-issuing thread
   uint64_t meta_full[2];  // key rows of a tile written: the meta warp's 32 lanes
   uint64_t meta_empty[2]; // key rows of a tile no longer needed: every softmax thread
-  uint64_t q_full;        // the token's Q rows landed (TMA)
+  uint64_t q_full;        // bf16: the token's Q rows landed (TMA)
   uint64_t pv_c0;         // PV issuer 0 has issued dv chunk 0 of a tile
   uint32_t tmem_base;
   int abort;
@@ -99,6 +124,8 @@ struct WideCtrl {
   int pf_ok[kWGroups];
   int need_rescale[kWGroups];
   int key_row[2][kTileKeys];  // KV row of each key of a tile, -1 = masked
+  // fp8: the four channel-group scales of each key of a tile (0 when masked)
+  float4 key_scale[FP8 ? 2 : 1][FP8 ? kTileKeys : 1];
   float red[kWGroups][4][32];
   alignas(16) float m_ref[R];
   alignas(16) float alpha[R];
@@ -107,20 +134,21 @@ struct WideCtrl {
   float sfac[R];  // merged output: sink factor per head
 };
 
-template <int R>
+template <bool FP8, int R>
 __host__ __device__ constexpr int wide_fixed_bytes() {
-  return 1024 + WideCfg<R>::kQBytes + WideCfg<R>::kPRegion + WideCfg<R>::kRopeSlot +
-         (int)sizeof(WideCtrl<R>);
+  return 1024 + WideCfg<FP8, R>::kQBytes + WideCfg<FP8, R>::kPRegion +
+         WideCfg<FP8, R>::kRopeSlot + (int)sizeof(WideCtrl<FP8, R>);
 }
-template <int R>
+// as many pair slots as fit (4 to 8)
+template <bool FP8, int R>
 __host__ __device__ constexpr int wide_slots() {
-  return (232448 - wide_fixed_bytes<R>()) / kWSlotBytes > 8
+  return (232448 - wide_fixed_bytes<FP8, R>()) / kWSlotBytes > 8
              ? 8
-             : (232448 - wide_fixed_bytes<R>()) / kWSlotBytes;
+             : (232448 - wide_fixed_bytes<FP8, R>()) / kWSlotBytes;
 }
-template <int R>
+template <bool FP8, int R>
 __host__ __device__ constexpr int wide_smem_bytes() {
-  return wide_fixed_bytes<R>() + wide_slots<R>() * kWSlotBytes;
+  return wide_fixed_bytes<FP8, R>() + wide_slots<FP8, R>() * kWSlotBytes;
 }
 
 constexpr unsigned long long kWDrainLimitNs = 20ull * 1000 * 1000;
@@ -132,25 +160,28 @@ __device__ __forceinline__ void wide_drain_wait(uint64_t *bar, uint32_t parity,
 }
 
 // MERGED: the epilogue writes the token's merged result (AttnArgs::o_out)
-// instead of the partial (o_part / lse_part).
-template <int R, bool MERGED>
-__global__ void __launch_bounds__(kWThreads, 1)
+// instead of the partial (o_part / lse_part).  tm_q (bf16) is Q as
+// [tokens, H, 576]; tm_rope (fp8) is the bf16 rope of the fp8 cache.
+template <bool FP8, int R, bool MERGED>
+__global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
     mla_sparse_wide_kernel(const __grid_constant__ AttnArgs a,
                            const __grid_constant__ CUtensorMap tm_kv,
-                           const __grid_constant__ CUtensorMap tm_q) {
-  using Cfg = WideCfg<R>;
+                           const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_rope) {
+  using Cfg = WideCfg<FP8, R>;
   constexpr int RC = Cfg::RC;
-  constexpr int NP = wide_slots<R>();
+  constexpr int NS = Cfg::NS;
+  constexpr int NP = wide_slots<FP8, R>();
   static_assert(NP >= kWPairs, "a tile needs four pair slots");
   static_assert(!Cfg::kRopeInP || NP == kWPairs, "the rope-in-P^T order assumes four slots");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *sQ = smem;                                 // 9 k-blocks of [R x 64] bf16
+  uint8_t *sQ = smem;                                 // 9 k-blocks of [R x 64] (fp8: latent fp16)
   uint8_t *sP = sQ + Cfg::kQBytes;                    // P^T (R = 64: also the rope)
   uint8_t *sRope = Cfg::kRopeInP ? sP : sP + Cfg::kPRegion;  // [128 keys x 64 dims]
   uint8_t *sRing = sP + Cfg::kPRegion + Cfg::kRopeSlot;      // NP pair slots
-  WideCtrl<R> &c = *reinterpret_cast<WideCtrl<R> *>(sRing + NP * kWSlotBytes);
+  WideCtrl<FP8, R> &c = *reinterpret_cast<WideCtrl<FP8, R> *>(sRing + NP * kWSlotBytes);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -166,21 +197,23 @@ __global__ void __launch_bounds__(kWThreads, 1)
     for (int s = 0; s < NP; ++s) {
       mbar_init(&c.full[s], kWGatherWarps);
       mbar_init(&c.empty[s], 1);
+      if (FP8)
+        for (int w = 0; w < kWGatherWarps; ++w) mbar_init(&c.raw[w][s], 1);
     }
     mbar_init(&c.rope_full, kWGatherWarps);
     mbar_init(&c.q_full, 1);
     mbar_init(&c.pv_c0, 1);
     mbar_init(&c.rope_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&c.s_full[s], 1);
+      mbar_init(&c.s_full[s], FP8 ? 2 : 1);
       mbar_init(&c.s_free[s], kWSoftmaxThreads);
       mbar_init(&c.meta_full[s], 32);
       mbar_init(&c.meta_empty[s], kWSoftmaxThreads);
     }
     mbar_init(&c.p_full, kWSoftmaxThreads);
-    mbar_init(&c.p_free, 2);
-    mbar_init(&c.o_full, 2);
-    for (int s = 0; s < 3; ++s) mbar_init(&c.drain[s], 1);
+    mbar_init(&c.p_free, Cfg::kPvIssuers);
+    mbar_init(&c.o_full, Cfg::kPvIssuers);
+    for (int s = 0; s < 8; ++s) mbar_init(&c.drain[s], 1);
     c.abort = 0;
     c.last_slot = -1;
     for (int g = 0; g < kWGroups; ++g) c.need_rescale[g] = 0;
@@ -206,7 +239,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, Cfg::kTmemCols);
   if (warp == kWGroup0 && lane == 0) tma_prefetch_desc(&tm_kv);
-  if (warp == 1 && lane == 0) tma_prefetch_desc(&tm_q);
+  if (warp == 1 && lane == 0) tma_prefetch_desc(FP8 ? &tm_rope : &tm_q);
   if (tid < R) {
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
@@ -216,14 +249,37 @@ __global__ void __launch_bounds__(kWThreads, 1)
   // outside its owner shard) computes nothing.
   const bool row_ok = c.row_ok != 0 && (!MERGED || c.gtok >= 0);
   const int64_t gq = row_ok ? (int64_t)a.rows[row] : -1;
-  // Q rows of this item: nine TMA boxes [R heads x 64 dims] straight into the
-  // MMA's K-major, 128-byte-swizzled k-blocks (heads past H read as zero);
-  // they land while the list is scanned and the first keys are gathered
-  if (tid == 0 && row_ok) {
-    mbar_arrive_expect_tx(&c.q_full, (uint32_t)(kKb * R * 128));
+  if (!FP8) {
+    // Q rows of this item: nine TMA boxes [R heads x 64 dims] straight into
+    // the MMA's K-major, 128-byte-swizzled k-blocks (heads past H read as
+    // zero); they land while the list is scanned and the first keys are
+    // gathered
+    if (tid == 0 && row_ok) {
+      mbar_arrive_expect_tx(&c.q_full, (uint32_t)(kKb * R * 128));
 #pragma unroll 1
-    for (int kb = 0; kb < kKb; ++kb)
-      tma_load_3d(sQ + kb * (R * 128), &tm_q, kb * kKbDims, h0, (int)gq, &c.q_full);
+      for (int kb = 0; kb < kKb; ++kb)
+        tma_load_3d(sQ + kb * (R * 128), &tm_q, kb * kKbDims, h0, (int)gq, &c.q_full);
+    }
+  } else {
+    // fp8: Q rows by the threads, the latent part converted to fp16 (it
+    // meets fp16 codes in the MMA; the rope part stays bf16 against the bf16
+    // rope), into the same K-major, 128-byte-swizzled k-blocks
+    constexpr int kChunks = R * (CPMLA_DQK / 8);  // 16-byte chunks
+    for (int idx = tid; idx < kChunks; idx += Cfg::kThreads) {
+      const int r = idx / (CPMLA_DQK / 8);
+      const int ch = idx - r * (CPMLA_DQK / 8);
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (row_ok && r < r_valid)
+        w = __ldg(reinterpret_cast<const uint4 *>(a.q + gq * a.q_stride +
+                                                  (int64_t)(h0 + r) * CPMLA_DQK) +
+                  ch);
+      if (ch < CPMLA_DV / 8)
+        w = make_uint4(bf16x2_to_f16x2(w.x), bf16x2_to_f16x2(w.y), bf16x2_to_f16x2(w.z),
+                       bf16x2_to_f16x2(w.w));
+      const int kb = ch >> 3, cc = ch & 7;
+      *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
+    }
+    fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
   }
   {
     // the last non-empty slot of the row's list: every thread scans its
@@ -232,7 +288,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int len = 0;
       const int32_t *lst = topk_window(a, row, gq, &len);
       int last = -1;
-      for (int e = tid; e < len; e += kWThreads)
+      for (int e = tid; e < len; e += Cfg::kThreads)
         if (__ldg(lst + e) >= 0) last = e;
       if (last >= 0) atomicMax(&c.last_slot, last);
     }
@@ -242,26 +298,35 @@ __global__ void __launch_bounds__(kWThreads, 1)
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
   const int n_tiles = (c.last_slot + kTileKeys) / kTileKeys;
-  const uint32_t tO = tmem + 2 * R;  // O^T chunk ch at tO + ch*R; S^T buffer b at tmem + b*R
+  // S^T buffer b at tmem + b*NS*R (fp8: accumulator g of it at + g*R, the
+  // rope at + 4R); O^T chunk ch at tO + ch*R
+  const uint32_t tO = tmem + 2 * NS * R;
   volatile int *abort = &c.abort;
 
-  if (warp == 0) {
-    // ---------------------------------------------------- score-GEMM issuer
+  if (warp == 0 || (FP8 && warp == kWScore2Warp)) {
+    // ---------------------------------------------------- score-GEMM issuer(s)
+    // bf16: warp 0 issues every MMA of a tile into one accumulator.  fp8:
+    // warp 0 the rope and pairs 0-1, warp 20 pairs 2-3, each into its own
+    // accumulators; s_full completes when both have committed.
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(128, R, 0, 0);
+      const bool second = FP8 && warp == kWScore2Warp;
+      constexpr uint32_t id_rope = idesc_bf16(128, R, 0, 0);
+      constexpr uint32_t id_lat = FP8 ? idesc_f16(128, R, 0, 0) : id_rope;
       // descriptors advance by (byte offset >> 4) in their address field
       const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
       const uint64_t drope = smem_desc(smem_u32(sRope), 16, 1024, kSwz128);
       const uint64_t dq_rope = dq0 + ((kLatKb * (R * 128)) >> 4);
-      bool ok = n_tiles == 0 || mbar_wait(&c.q_full, 0, abort, a.status);
+      const int p_lo = second ? 2 : 0;
+      const int p_hi = FP8 ? (second ? 4 : 2) : kWPairs;
+      bool ok = FP8 || n_tiles == 0 || mbar_wait(&c.q_full, 0, abort, a.status);
       for (int i = 0; i < n_tiles && ok; ++i) {
-        const uint32_t dS = tmem + (i & 1) * R;
+        const uint32_t dS = tmem + (i & 1) * NS * R;
         if (i >= 2 && !mbar_wait(&c.s_free[i & 1], ((i >> 1) - 1) & 1, abort, a.status)) {
           ok = false;
           break;
         }
-        if (!Cfg::kRopeInP) {
+        if (!Cfg::kRopeInP && !second) {
           // the rope first (it starts the accumulator), then its slot is free
           if (!mbar_wait(&c.rope_full, i & 1, abort, a.status)) {
             ok = false;
@@ -270,11 +335,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int st = 0; st < 4; ++st)
-            mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_qk,
-                        st == 0 ? 0u : 1u);
+            mma_bf16_ss(dS + (FP8 ? 4 * R : 0), drope + ((st * 32) >> 4),
+                        dq_rope + ((st * 32) >> 4), id_rope, st == 0 ? 0u : 1u);
           mma_commit(&c.rope_empty);
         }
-        for (int p = 0; p < kWPairs; ++p) {
+        for (int p = p_lo; p < p_hi; ++p) {
           if (Cfg::kRopeInP && p == 2) {
             // the rope (gathered after pair 1, into the P^T region once the
             // PV GEMM of the previous tile has read it) before the last pairs
@@ -285,7 +350,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int st = 0; st < 4; ++st)
-              mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_qk, 1u);
+              mma_bf16_ss(dS, drope + ((st * 32) >> 4), dq_rope + ((st * 32) >> 4), id_rope, 1u);
           }
           const uint32_t pos = 4u * i + p, slot = pos % NP;
           if (!mbar_wait(&c.full[slot], (pos / NP) & 1, abort, a.status)) {
@@ -295,32 +360,36 @@ __global__ void __launch_bounds__(kWThreads, 1)
           tc_fence_after();
           const uint64_t da = dr0 + ((slot * kWSlotBytes) >> 4);
           const uint64_t db = dq0 + ((2 * p * (R * 128)) >> 4);
+          const uint32_t d_acc = FP8 ? dS + p * R : dS;  // fp8: scale group p
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t h = k >> 2, st = k & 3;
-            mma_bf16_ss(dS, da + ((h * kKbBytes + st * 32) >> 4),
-                        db + ((h * (R * 128) + st * 32) >> 4), id_qk,
-                        (!Cfg::kRopeInP || (p | k) != 0) ? 1u : 0u);
+            const bool acc = FP8 ? k != 0 : (!Cfg::kRopeInP || (p | k) != 0);
+            mma_bf16_ss(d_acc, da + ((h * kKbBytes + st * 32) >> 4),
+                        db + ((h * (R * 128) + st * 32) >> 4), id_lat, acc ? 1u : 0u);
           }
         }
         if (!ok) break;
         mma_commit(&c.s_full[i & 1]);
       }
+      uint64_t *drain = &c.drain[second ? 1 : 0];
       if (!ok) {
-        mma_commit(&c.drain[0]);
-        wide_drain_wait(&c.drain[0], 0, kWaitLimitNs);
+        mma_commit(drain);
+        wide_drain_wait(drain, 0, kWaitLimitNs);
       }
       // the Q copy this thread issued has landed before the CTA can exit
-      if (row_ok) wide_drain_wait(&c.q_full, 0, kWaitLimitNs);
+      if (!FP8 && row_ok) wide_drain_wait(&c.q_full, 0, kWaitLimitNs);
     }
     __syncwarp();
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 1 || warp == 2 || (FP8 && (warp == kWPv2Warp || warp == kWPv2Warp + 1))) {
     // ---------------------------------------------------- PV-GEMM issuers
     // O^T chunk ch += V^T . P^T from tile j's resident pair ch, which is then
-    // released; issuer `me` takes chunks me and me + 2
+    // released.  bf16: issuer `me` takes chunks me and me + 2; fp8: four
+    // issuers (warps 1, 2, 21, 22), one chunk each, with the P^T of chunk ch
+    // that carries that chunk's scales
     if (lane == 0) {
-      const int me = warp - 1;
-      constexpr uint32_t id_pv = idesc_bf16(128, R, 1, 1);
+      const int me = warp <= 2 ? warp - 1 : warp - kWPv2Warp + 2;
+      constexpr uint32_t id_pv = FP8 ? idesc_f16(128, R, 1, 1) : idesc_bf16(128, R, 1, 1);
       const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 8 * PLayout<R>::row_bytes,
                                      PLayout<R>::swz);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
@@ -333,35 +402,36 @@ __global__ void __launch_bounds__(kWThreads, 1)
         tc_fence_after();
         // chunk 0 reaches the tensor core before the other issuer's first
         // chunk, so the first ring slot of the tile is freed soonest
-        if (me == 1 && !mbar_wait(&c.pv_c0, j & 1, abort, a.status)) {
+        if (Cfg::kPvIssuers == 2 && me == 1 && !mbar_wait(&c.pv_c0, j & 1, abort, a.status)) {
           ok = false;
           break;
         }
-        for (int ch = me; ch < kWPairs; ch += 2) {
+        for (int ch = me; ch < kWPairs; ch += Cfg::kPvIssuers) {
           const uint32_t slot = (4u * j + ch) % NP;
           const uint64_t da = dr0 + ((slot * kWSlotBytes) >> 4);
+          const uint32_t pm = FP8 ? ch * Cfg::kPBytes : 0;
 #pragma unroll
           for (int st = 0; st < kTileKeys / 16; ++st)
             mma_bf16_ss(tO + ch * R, da + ((st * 2048) >> 4),
-                        dp0 + ((st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
+                        dp0 + ((pm + st * 16 * PLayout<R>::row_bytes) >> 4), id_pv,
                         (j > 0 || st > 0) ? 1u : 0u);
           mma_commit(&c.empty[slot]);
-          if (ch == 0) mbar_arrive(&c.pv_c0);
+          if (Cfg::kPvIssuers == 2 && ch == 0) mbar_arrive(&c.pv_c0);
         }
         mma_commit(&c.p_free);
       }
       mma_commit(&c.o_full);
       if (!ok) {
-        mma_commit(&c.drain[1 + me]);
-        wide_drain_wait(&c.drain[1 + me], 0, kWaitLimitNs);
+        mma_commit(&c.drain[2 + me]);
+        wide_drain_wait(&c.drain[2 + me], 0, kWaitLimitNs);
       }
     }
     __syncwarp();
   } else if (warp == kWMetaWarp) {
     // ---------------------------------------------------- key rows
     // key t of tile j: its KV row, or -1 when the slot is empty or outside
-    // the row's range; the list entries of tile j+1 load while tile j's are
-    // resolved
+    // the row's range (fp8: and its four scales); the list entries of tile
+    // j+1 load while tile j's are resolved
     if (row_ok && n_tiles > 0) {
       const int tpos = a.pos[row];
       const int64_t base = a.kv_start[a.req[row]];
@@ -383,6 +453,25 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const int e = (j + 1) * kTileKeys + q * 32 + lane;
           nxt[q] = (j + 1 < n_tiles && e < len) ? __ldg(lst + e) : -1;
         }
+        int src[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int p = cur[q];
+          src[q] = -1;
+          if (p >= 0) {
+            if (p > tpos || base + p >= a.s_kv)
+              record_status(a.status, CPMLA_ERR_INDEX);
+            else if (p >= lo && p <= hi)
+              src[q] = (int)(base + p);
+          }
+        }
+        float4 sc[4];
+        if (FP8) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            sc[q] = src[q] >= 0 ? __ldg(reinterpret_cast<const float4 *>(a.kv_scale) + src[q])
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         // the softmax of tile j-2 (and with it every gather of that tile)
         // must be done with this buffer
         if (j >= 2) {
@@ -394,21 +483,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int p = cur[q];
-          int src = -1;
-          if (p >= 0) {
-            if (p > tpos || base + p >= a.s_kv)
-              record_status(a.status, CPMLA_ERR_INDEX);
-            else if (p >= lo && p <= hi)
-              src = (int)(base + p);
-          }
-          c.key_row[j & 1][q * 32 + lane] = src;
+          c.key_row[j & 1][q * 32 + lane] = src[q];
+          if (FP8) c.key_scale[FP8 ? (j & 1) : 0][FP8 ? q * 32 + lane : 0] = sc[q];
         }
         mbar_arrive(&c.meta_full[j & 1]);
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kWGroup0 && warp < kWGroup0 + kWGatherWarps) {
     // ---------------------------------------------------- softmax + gathers
     const int gw = warp - kWGroup0;  // gather warp 0..15
     const int grp = gw >> 2;         // softmax warpgroup
@@ -435,20 +517,33 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (lane == 0) r = mbar_wait(bar, parity, abort, a.status) ? 1 : 0;
       gok = __shfl_sync(0xffffffffu, r, 0) != 0;
     };
-    // My share of one gather unit.  Pair slot: keys 16 (gw % 8) .. +15 of
-    // k-block gw / 8 (4 four-row gathers); rope: keys 8 gw .. 8 gw + 7 (2).
-    // A masked key fetches KV row 0, which the softmax gives weight exactly 0.
+    // My share of one gather unit.  bf16 pair slot: keys 16 (gw % 8) .. +15
+    // of k-block gw / 8 (4 four-row gathers); fp8 pair slot: the raw codes of
+    // keys 8 gw .. 8 gw + 7 (2; 128 B a key, unswizzled, in the upper half of
+    // the slot); rope: keys 8 gw .. 8 gw + 7 (2).  A masked key fetches KV row
+    // 0, which the softmax gives weight exactly 0.
     auto gather = [&](bool rope, int tile, int pr, uint8_t *dst, uint64_t *bar, uint32_t par) {
       const int *krow = c.key_row[tile & 1];
-      const int k0 = rope ? 8 * gw : 16 * (gw & 7);
-      const int n4 = rope ? 2 : 4;
-      uint8_t *d = rope ? dst + gw * 1024 : dst + (gw >> 3) * kKbBytes + (gw & 7) * 2048;
-      const int x = rope ? CPMLA_DV : pr * 128 + (gw >> 3) * kKbDims;
+      int k0, n4, x;
+      uint8_t *d;
+      const CUtensorMap *tm = &tm_kv;
+      if (FP8) {
+        k0 = 8 * gw;
+        n4 = 2;
+        d = rope ? dst + gw * 1024 : dst + kKbBytes + gw * 1024;
+        x = rope ? 0 : pr * 128;
+        if (rope) tm = &tm_rope;
+      } else {
+        k0 = rope ? 8 * gw : 16 * (gw & 7);
+        n4 = rope ? 2 : 4;
+        d = rope ? dst + gw * 1024 : dst + (gw >> 3) * kKbBytes + (gw & 7) * 2048;
+        x = rope ? CPMLA_DV : pr * 128 + (gw >> 3) * kKbDims;
+      }
       if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)n4 * 512);
       __syncwarp();
       if (lane < n4) {
         const int *kr = krow + k0 + 4 * lane;
-        tma_gather4(d + lane * 512, &tm_kv, x, kr[0] >= 0 ? kr[0] : 0, kr[1] >= 0 ? kr[1] : 0,
+        tma_gather4(d + lane * 512, tm, x, kr[0] >= 0 ? kr[0] : 0, kr[1] >= 0 ? kr[1] : 0,
                     kr[2] >= 0 ? kr[2] : 0, kr[3] >= 0 ? kr[3] : 0, bar);
       }
       __syncwarp();
@@ -458,17 +553,62 @@ __global__ void __launch_bounds__(kWThreads, 1)
     };
     // Pair pr of tile j into its ring slot, once the slot's previous use has
     // been released by its PV GEMM (that tile's softmax is always done by
-    // the time this is called).
+    // the time this is called).  fp8: the codes land on this warp's own
+    // barrier and are converted by convert_pair.
     auto gather_pair = [&](int j, int pr) {
       const int p = 4 * j + pr;
       if (gok && p >= NP) wwait(&c.empty[p % NP], ((p - NP) / NP) & 1);
-      if (gok) gather(false, j, pr, sRing + (p % NP) * kWSlotBytes, &c.full[p % NP], (p / NP) & 1);
+      if (gok)
+        gather(false, j, pr, sRing + (p % NP) * kWSlotBytes,
+               FP8 ? &c.raw[FP8 ? gw : 0][p % NP] : &c.full[p % NP], (p / NP) & 1);
+    };
+    // fp8: this warp's keys of pair pr of tile j, once their codes have
+    // landed, converted in place from the raw codes (key k at 16 KB + 128 k)
+    // to fp16 in the two 128-byte-swizzled k-blocks; the key's k-block-1 row
+    // lies over its own codes, so the warp reads all its codes before it
+    // writes.  Unit u of the warp = key 8 gw + u / 8, codes 16 (u % 8) ...
+    auto convert_pair = [&](int j, int pr) {
+      const int p = 4 * j + pr;
+      if (gok) wwait(&c.raw[FP8 ? gw : 0][p % NP], (p / NP) & 1);
+      if (!gok) return;
+      __syncwarp();
+      uint8_t *sl = sRing + (p % NP) * kWSlotBytes;
+      uint4 w4[2];
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int u = lane + 32 * b;
+        w4[b] = *reinterpret_cast<const uint4 *>(sl + kKbBytes + (8 * gw + (u >> 3)) * 128 +
+                                                 (u & 7) * 16);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int u = lane + 32 * b;
+        const int key = 8 * gw + (u >> 3), c8 = u & 7;
+        const uint32_t w[4] = {w4[b].x, w4[b].y, w4[b].z, w4[b].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          o[2 * q] = e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu));
+          o[2 * q + 1] = e4m3x2_to_f16x2((uint16_t)(w[q] >> 16));
+        }
+        // dims 16 c8 .. 16 c8 + 15 of the pair: k-block c8 / 4, chunks 2 (c8 % 4), +1
+        const int kb = c8 >> 2, cc0 = 2 * (c8 & 3);
+        uint8_t *rowp = sl + kb * kKbBytes + key * 128;
+        *reinterpret_cast<uint4 *>(rowp + ((cc0 ^ (key & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(rowp + (((cc0 + 1) ^ (key & 7)) << 4)) =
+            make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      fence_proxy_async_smem();  // written by threads, read by tcgen05.mma
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.full[p % NP]);
     };
     auto gather_meta = [&](int j) {
       if (gok) wwait(&c.meta_full[j & 1], (j >> 1) & 1);
     };
-    // rope of tile j: its own slot (R = 32; read first by the score GEMM of
-    // tile j-1), or the P^T region once PV(j-1) is done (R = 64)
+    // rope of tile j: its own slot (R = 32, fp8; read first by the score GEMM
+    // of tile j-1), or the P^T region once PV(j-1) is done (R = 64)
     auto gather_rope = [&](int j) {
       if (j >= 1 && gok) {
         if (Cfg::kRopeInP)
@@ -479,27 +619,81 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (gok) gather(true, j, 0, sRope, &c.rope_full, j & 1);
     };
 
-    // Softmax of tile j for this warpgroup's columns; false when the CTA
-    // gave up.
-    auto ld_cols = [&](uint32_t col, float *v) {
+    // TMEM columns of this warpgroup (RC of them) without the wait
+    auto ld_cols_nw = [&](uint32_t col, float *v) {
       if (RC == 16) {
         tmem_ld16(col, v);
-      } else {
+      } else if (RC == 8) {
         tmem_ld8(col, v);
+      } else {
+        tmem_ld4(col, v);
       }
+    };
+    auto st_cols = [&](uint32_t col, const float *v) {
+      if (RC == 16) {
+        tmem_st16(col, v);
+      } else if (RC == 8) {
+        tmem_st8(col, v);
+      } else {
+        tmem_st4(col, v);
+      }
+    };
+    auto ld_cols = [&](uint32_t col, float *v) {
+      ld_cols_nw(col, v);
       tmem_ld_wait();
     };
+    // P^T row of key t, this group's RC columns, 16-byte chunks swizzled
+    auto store_p = [&](uint8_t *pbase, const uint32_t *pk) {
+      uint8_t *prow = pbase + t * PLayout<R>::row_bytes;
+      if (RC >= 8) {
+#pragma unroll
+        for (int ch = 0; ch < RC / 8; ++ch) {
+          const int phys = (grp * (RC / 8) + ch) ^ PLayout<R>::chunk_xor(t);
+          *reinterpret_cast<uint4 *>(prow + phys * 16) =
+              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        }
+      } else {
+        // four columns: half of a 16-byte chunk
+        const int phys = (grp >> 1) ^ PLayout<R>::chunk_xor(t);
+        *reinterpret_cast<uint2 *>(prow + phys * 16 + (grp & 1) * 8) = make_uint2(pk[0], pk[1]);
+      }
+    };
+
+    // Softmax of tile j for this warpgroup's columns; false when the CTA
+    // gave up.
     auto softmax = [&](int j) -> bool {
       const int sb = j & 1;
       if (!group_wait(&c.s_full[sb], (j >> 1) & 1, t, bar_id, c.bflag[grp], seq, abort,
                       a.status))
         return false;
       tc_fence_after();
-      const uint32_t tS = tmem + sb * R + lane_off + cbase;
+      const uint32_t tS = tmem + sb * NS * R + lane_off + cbase;
       // x = score * scale * log2(e) - reference (base 2), -inf for a masked
       // key or a padding head; a reference still at -inf gives +inf
       float x[RC];
-      ld_cols(tS, x);
+      float s8[FP8 ? RC : 1];     // fp8: the scores, kept for a move of the reference
+      float ksc[4] = {1.f, 1.f, 1.f, 1.f};  // fp8: this key's group scales
+      if (!FP8) {
+        ld_cols(tS, x);
+      } else {
+        // s = rope part + sum_g scale_g * (q . E4M3 codes of group g)
+        const float4 sc4 = c.key_scale[FP8 ? sb : 0][FP8 ? t : 0];
+        ksc[0] = sc4.x;
+        ksc[1] = sc4.y;
+        ksc[2] = sc4.z;
+        ksc[3] = sc4.w;
+        float part[4][RC];
+        ld_cols_nw(tS + 4 * R, x);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) ld_cols_nw(tS + g * R, part[g]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int r = 0; r < RC; ++r) {
+          x[r] += ksc[0] * part[0][r] + ksc[1] * part[1][r] + ksc[2] * part[2][r] +
+                  ksc[3] * part[3][r];
+          s8[FP8 ? r : 0] = x[r];
+        }
+      }
       const bool valid = c.key_row[sb][t] >= 0;
       float m[RC];
 #pragma unroll
@@ -525,9 +719,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
       const bool move = named_bar_or(bar_id, 128, mx > 8.f);
       if (!*reinterpret_cast<volatile int *>(&c.pf_ok[grp])) return false;
       if (move) {
-        // the scores again, for each column's tile maximum
+        // the scores again (bf16: from TMEM), for each column's tile maximum
         float v[RC];
-        ld_cols(tS, v);
+        if (FP8) {
+#pragma unroll
+          for (int r = 0; r < RC; ++r) v[r] = s8[FP8 ? r : 0];
+        } else {
+          ld_cols(tS, v);
+        }
 #pragma unroll
         for (int r = 0; r < RC; ++r) {
           v[r] = (valid && cbase + r < r_valid) ? v[r] * a.scale_log2 : -INFINITY;
@@ -563,9 +762,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
       for (int r = 0; r < RC; r += 2) {
         const float p0 = fast_exp2(x[r]);
         const float p1 = fast_exp2(x[r + 1]);
-        pk[r / 2] = pack_bf16x2(p0, p1);
+        if (!FP8) pk[r / 2] = pack_bf16x2(p0, p1);
         l_part[r] += p0;
         l_part[r + 1] += p1;
+        x[r] = p0;
+        x[r + 1] = p1;
       }
       const bool rescale = move && c.need_rescale[grp] == j + 1;
       tc_fence_after();
@@ -574,29 +775,25 @@ __global__ void __launch_bounds__(kWThreads, 1)
         for (int ch = 0; ch < 4; ++ch) {
           float o[RC];
           const uint32_t col = tO + lane_off + ch * R + cbase;
-          if (RC == 16) {
-            tmem_ld16(col, o);
-          } else {
-            tmem_ld8(col, o);
-          }
-          tmem_ld_wait();
+          ld_cols(col, o);
 #pragma unroll
-          for (int x = 0; x < RC; ++x) o[x] *= c.alpha[cbase + x];
-          if (RC == 16) {
-            tmem_st16(col, o);
-          } else {
-            tmem_st8(col, o);
-          }
+          for (int y = 0; y < RC; ++y) o[y] *= c.alpha[cbase + y];
+          st_cols(col, o);
         }
         tmem_st_wait();
       }
-      // P^T row of key t: this group's RC columns, 16-byte chunks swizzled
-      uint8_t *prow = sP + t * PLayout<R>::row_bytes;
+      if (!FP8) {
+        store_p(sP, pk);
+      } else {
+        // P^T of dv chunk ch: p times this key's scale of channel group ch,
+        // in fp16 (11 significant bits) against the fp16 codes
 #pragma unroll
-      for (int ch = 0; ch < RC / 8; ++ch) {
-        const int phys = (grp * (RC / 8) + ch) ^ PLayout<R>::chunk_xor(t);
-        *reinterpret_cast<uint4 *>(prow + phys * 16) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+          for (int r = 0; r < RC; r += 2)
+            pk[r / 2] = pack_f16x2(x[r] * ksc[ch], x[r + 1] * ksc[ch]);
+          store_p(sP + ch * Cfg::kPBytes, pk);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -608,16 +805,29 @@ __global__ void __launch_bounds__(kWThreads, 1)
     // The sequence: tile j's gathers, then its softmax.  Ring position p
     // reuses the slot of position p - NP, released by the PV GEMM of that
     // tile, which follows that tile's softmax -- done one iteration earlier.
-    // R = 32 (five slots): the rope and pair 0 of tile j+1 wait for nothing
-    // and land while the PV GEMM of tile j frees the other slots.  R = 64:
-    // the rope goes after pair 1 (the PV GEMM of tile j-1 is done by then),
-    // so the score GEMM's tail only waits for pairs 2 and 3.
+    // R = 32 and fp8 (five slots): the rope and pair 0 of tile j+1 wait for
+    // nothing and land while the PV GEMM of tile j frees the other slots.
+    // R = 64: the rope goes after pair 1 (the PV GEMM of tile j-1 is done by
+    // then), so the score GEMM's tail only waits for pairs 2 and 3.  fp8:
+    // each pair is converted once its codes have landed, one pair behind the
+    // gathers.
     for (int j = 0; j < n_tiles && ok; ++j) {
       gather_meta(j);
       if (!Cfg::kRopeInP) gather_rope(j);
-      for (int pr = 0; pr < kWPairs; ++pr) {
-        gather_pair(j, pr);
-        if (Cfg::kRopeInP && pr == 1) gather_rope(j);
+      if (FP8) {
+        gather_pair(j, 0);
+        gather_pair(j, 1);
+        convert_pair(j, 0);
+        gather_pair(j, 2);
+        convert_pair(j, 1);
+        gather_pair(j, 3);
+        convert_pair(j, 2);
+        convert_pair(j, 3);
+      } else {
+        for (int pr = 0; pr < kWPairs; ++pr) {
+          gather_pair(j, pr);
+          if (Cfg::kRopeInP && pr == 1) gather_rope(j);
+        }
       }
       ok = softmax(j);
     }
@@ -657,22 +867,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
       for (int ch = 0; ch < 4; ++ch) {
         float o[RC];
         if (n_tiles > 0) {
-          if (RC == 16) {
-            tmem_ld16(tO + lane_off + ch * R + cbase, o);
-          } else {
-            tmem_ld8(tO + lane_off + ch * R + cbase, o);
-          }
-          tmem_ld_wait();
+          ld_cols(tO + lane_off + ch * R + cbase, o);
         } else {
 #pragma unroll
-          for (int x = 0; x < RC; ++x) o[x] = 0.f;
+          for (int y = 0; y < RC; ++y) o[y] = 0.f;
         }
         if (!MERGED) {
 #pragma unroll
-          for (int x = 0; x < RC; ++x) {
-            const int r = cbase + x;
+          for (int y = 0; y < RC; ++y) {
+            const int r = cbase + y;
             if (r >= r_valid || !row_ok) continue;
-            a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] = o[x] * c.inv_l[r];
+            a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] = o[y] * c.inv_l[r];
           }
         } else {
           // merged: bf16 pairs of neighbouring dv -- lane pairs trade one
@@ -682,10 +887,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
           const bool odd = (lane & 1) != 0;
           const bool own = row_ok && c.gtok >= 0;
 #pragma unroll
-          for (int x = 0; x < RC; x += 2) {
-            const int r = cbase + x;
-            const float v0 = r < r_valid ? (o[x] * c.inv_l[r]) * c.sfac[r] : 0.f;
-            const float v1 = r + 1 < r_valid ? (o[x + 1] * c.inv_l[r + 1]) * c.sfac[r + 1] : 0.f;
+          for (int y = 0; y < RC; y += 2) {
+            const int r = cbase + y;
+            const float v0 = r < r_valid ? (o[y] * c.inv_l[r]) * c.sfac[r] : 0.f;
+            const float v1 = r + 1 < r_valid ? (o[y + 1] * c.inv_l[r + 1]) * c.sfac[r + 1] : 0.f;
             const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
             const int hr = odd ? r + 1 : r;
             if (own && hr < r_valid) {
@@ -708,15 +913,15 @@ __global__ void __launch_bounds__(kWThreads, 1)
   }
 }
 
-template <int R, bool MERGED>
+template <bool FP8, int R, bool MERGED>
 int launch_wide_t(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &tm_q,
-                  int n_items, cudaStream_t stream) {
-  constexpr int smem = wide_smem_bytes<R>();
+                  const CUtensorMap &tm_rope, int n_items, cudaStream_t stream) {
+  constexpr int smem = wide_smem_bytes<FP8, R>();
   static_assert(smem <= 232448, "shared memory budget");
-  auto kern = mla_sparse_wide_kernel<R, MERGED>;
+  auto kern = mla_sparse_wide_kernel<FP8, R, MERGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: set shared memory size");
-  kern<<<n_items, kWThreads, smem, stream>>>(args, tm_kv, tm_q);
+  kern<<<n_items, WideCfg<FP8, R>::kThreads, smem, stream>>>(args, tm_kv, tm_q, tm_rope);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention: launch");
   return CPMLA_OK;
@@ -724,13 +929,19 @@ int launch_wide_t(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensor
 
 }  // namespace
 
-int launch_sparse_wide(int R, const AttnArgs &args, const CUtensorMap &tm_kv,
-                       const CUtensorMap &tm_q, int n_items, cudaStream_t st) {
+int launch_sparse_wide(bool fp8, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
+                       const CUtensorMap &tm_q, const CUtensorMap &tm_rope, int n_items,
+                       cudaStream_t st) {
+  if (fp8) {
+    if (R != 16) return fail(CPMLA_ERR_UNSUPPORTED, "sparse attention: fp8 takes 16 heads a CTA");
+    return args.o_out ? launch_wide_t<true, 16, true>(args, tm_kv, tm_q, tm_rope, n_items, st)
+                      : launch_wide_t<true, 16, false>(args, tm_kv, tm_q, tm_rope, n_items, st);
+  }
   if (args.o_out)
-    return R == 64 ? launch_wide_t<64, true>(args, tm_kv, tm_q, n_items, st)
-                   : launch_wide_t<32, true>(args, tm_kv, tm_q, n_items, st);
-  return R == 64 ? launch_wide_t<64, false>(args, tm_kv, tm_q, n_items, st)
-                 : launch_wide_t<32, false>(args, tm_kv, tm_q, n_items, st);
+    return R == 64 ? launch_wide_t<false, 64, true>(args, tm_kv, tm_q, tm_rope, n_items, st)
+                   : launch_wide_t<false, 32, true>(args, tm_kv, tm_q, tm_rope, n_items, st);
+  return R == 64 ? launch_wide_t<false, 64, false>(args, tm_kv, tm_q, tm_rope, n_items, st)
+                 : launch_wide_t<false, 32, false>(args, tm_kv, tm_q, tm_rope, n_items, st);
 }
 
 }  // namespace cpmla
