@@ -725,9 +725,7 @@ def main():
                      "peak": pk["bf16"], "unit": "TFLOP/s",
                      "frac": round(attn_tflops / pk["bf16"], 4),
                      "traffic": NCU_TRAFFIC_BYTES.get((args.workload, args.path)),
-                     "kernel": ("mla_dense_kernel" if not prob.topk else
-                                "mla_sparse_kernel" if prob.kv_format == "fp8" or prob.H <= 16
-                                else "mla_sparse_wide_kernel"),
+                     "kernel": "mla_dense_kernel" if not prob.topk else "mla_sparse_wide_kernel",
                      "peak_source": pk["source"] + " burst bf16"},
         "merge_roofline": {"bound": "hbm", "achieved": round(merge_gbs, 1), "peak": pk["hbm"],
                            "unit": "GB/s", "frac": round(merge_gbs / pk["hbm"], 4),

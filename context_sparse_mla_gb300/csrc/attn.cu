@@ -11,7 +11,7 @@
 // their epilogue for the query-partitioned case, where every token has one
 // partial: its owner row applies the sink once and writes bf16 O and the LSE
 // in global token order, the merge kernel's arithmetic for one partial.  The
-// kernels live in attn_dense.cu and attn_sparse.cu.
+// kernels live in attn_dense.cu and attn_sparse_wide.cu.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -134,9 +134,8 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   } else {
     // one token per CTA.  fp8 works on 16 heads at a time (its four P^T
     // matrices and five score accumulators are sized for R = 16); bf16 takes
-    // up to 16 heads in the narrow kernel, up to 32 or 64 in the wide one
-    // (all heads of a 64-head token in one CTA, so its keys are gathered
-    // once)
+    // up to 64 (all heads of a 64-head token in one CTA, so its keys are
+    // gathered once)
     const int hmax = kv_format == CPMLA_KV_FP8_E4M3_G128 ? 16 : 64;
     args.hc = H <= hmax ? H : hmax;
     if (H > hmax && H % hmax != 0)
@@ -184,7 +183,7 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
     }
     if (cr2 != CUDA_SUCCESS)
       return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr2);
-    if (kv_format == CPMLA_KV_BF16 && R > 16) {
+    if (kv_format == CPMLA_KV_BF16) {
       // Q as [T tokens, H heads, 576] with the token stride; one box is the
       // 64 dims of one k-block for R consecutive heads of one token, in the
       // MMA's 128-byte-swizzled K-major layout (heads past H read as zero)
@@ -204,9 +203,7 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
         return fail(CPMLA_ERR_CUDA, "%s: Q tensor map encode failed (%d)", fn, (int)cq);
       return launch_sparse_wide(false, R, args, tm_kv, tm_q, tm_rope, (int)n_items, st);
     }
-    if (kv_format == CPMLA_KV_FP8_E4M3_G128)
-      return launch_sparse_wide(true, 16, args, tm_kv, tm_kv, tm_rope, (int)n_items, st);
-    return launch_sparse(kSparseBf16, R, args, tm_kv, tm_rope, (int)n_items, st);
+    return launch_sparse_wide(true, 16, args, tm_kv, tm_kv, tm_rope, (int)n_items, st);
   }
   // 128-key x 64-dim tiles of the bf16 KV
   CUtensorMap tm;

@@ -23,8 +23,6 @@ constexpr int kKbBytes = kTileKeys * kKbDims * 2;  // 16 KB
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;
 
-enum Mode { kDense = 0, kSparseBf16 = 1, kSparseFp8 = 2 };
-
 struct AttnArgs {
   const __nv_bfloat16 *q;
   int64_t q_stride;  // elements between tokens
@@ -197,15 +195,12 @@ int launch_merge_to_tokens(const float *o_part, const float *lse_part, int64_t n
 
 // Launchers (one per translation unit); n_items CTAs, one work item each.
 int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st);
-// Sparse: one-row gather maps.  bf16: tm_kv = tm_rope = the KV (box 64 x 1,
-// 128-byte swizzle).  fp8: tm_kv = the E4M3 codes (box 128 x 1, no swizzle),
-// tm_rope = the bf16 rope (box 64 x 1, 128-byte swizzle).
-int launch_sparse(int mode, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
-                  const CUtensorMap &tm_rope, int n_items, cudaStream_t st);
-// Sparse with 16 gather warps (attn_sparse_wide.cu): bf16 KV with R = 32 or
-// 64 heads per CTA, or fp8 KV with R = 16.  tm_kv and tm_rope as for
-// launch_sparse; bf16: tm_q = Q as [T, H, 576] in boxes of 64 dims x R heads
-// x 1 token, 128-byte swizzle (fp8 reads Q with plain loads; tm_q unused).
+// Sparse (attn_sparse_wide.cu): bf16 KV with R = 16, 32 or 64 heads per CTA,
+// or fp8 KV with R = 16.  One-row gather maps: bf16: tm_kv = tm_rope = the
+// KV (box 64 x 1, 128-byte swizzle); fp8: tm_kv = the E4M3 codes (box 128 x
+// 1, no swizzle), tm_rope = the bf16 rope (box 64 x 1, 128-byte swizzle).
+// bf16: tm_q = Q as [T, H, 576] in boxes of 64 dims x R heads x 1 token,
+// 128-byte swizzle (fp8 reads Q with plain loads; tm_q unused).
 int launch_sparse_wide(bool fp8, int R, const AttnArgs &args, const CUtensorMap &tm_kv,
                        const CUtensorMap &tm_q, const CUtensorMap &tm_rope, int n_items,
                        cudaStream_t st);

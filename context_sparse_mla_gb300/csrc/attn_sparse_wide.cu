@@ -1,5 +1,5 @@
 // attn_sparse_wide.cu -- top-k sparse partial MLA attention (output + LSE, no
-// sink) for one token per CTA, on sm_103a: a bf16 latent KV for 17 to 64
+// sink) for one token per CTA, on sm_103a: a bf16 latent KV for up to 64
 // heads, or the fp8 KV cache (E4M3 latent with one scale per 128 channels,
 // bf16 rope) for 16 heads at a time.
 //
@@ -10,7 +10,7 @@
 // "[Feature][PCP] Add DeepSeek-V4.1-Flash support", "Supported Scope": the
 // sparse MLA path with an fp8 KV cache.
 //
-// One CTA = one token x R heads (bf16: R = 32 or 64; fp8: R = 16).  A token's
+// One CTA = one token x R heads (bf16: R = 16, 32 or 64; fp8: R = 16).  A token's
 // keys are its own, so every gathered key row feeds only this token's heads:
 // with R = 64 one CTA covers all heads of a 64-head token and each key row is
 // gathered once.
@@ -20,7 +20,7 @@
 //     used (the latent is the value, so it stays resident).
 //   * Shared memory: Q [R x 576], P^T [128 keys x R], a ring of NP 32 KB pair
 //     slots (two k-blocks [128 keys x 64 dims]); pair p of tile j at ring
-//     position 4j + p.  R = 32: a rope slot of its own and five pair slots, so
+//     position 4j + p.  R = 16, 32: a rope slot of its own and five pair slots, so
 //     the rope and first pair of tile j+2 are gathered while tile j+1 still
 //     waits for its softmax.  R = 64 (Q alone is 72 KB): four pair slots, and
 //     the rope k-block shares the region of P^T -- the rope of tile j+1 is
@@ -80,7 +80,8 @@ constexpr int kWRec = 6;                   // gathers remembered per warp for th
 
 template <bool FP8, int R>
 struct WideCfg {
-  static_assert(FP8 ? R == 16 : (R == 32 || R == 64), "bf16: 32 or 64 heads per CTA; fp8: 16");
+  static_assert(FP8 ? R == 16 : (R == 16 || R == 32 || R == 64),
+                "bf16: 16, 32 or 64 heads per CTA; fp8: 16");
   static constexpr int RC = R / kWGroups;            // score columns per softmax warpgroup
   static constexpr int NS = FP8 ? 5 : 1;             // score accumulators per S^T buffer
   static constexpr bool kRopeInP = !FP8 && R == 64;  // rope shares the P^T region
@@ -938,10 +939,12 @@ int launch_sparse_wide(bool fp8, int R, const AttnArgs &args, const CUtensorMap 
                       : launch_wide_t<true, 16, false>(args, tm_kv, tm_q, tm_rope, n_items, st);
   }
   if (args.o_out)
-    return R == 64 ? launch_wide_t<false, 64, true>(args, tm_kv, tm_q, tm_rope, n_items, st)
-                   : launch_wide_t<false, 32, true>(args, tm_kv, tm_q, tm_rope, n_items, st);
-  return R == 64 ? launch_wide_t<false, 64, false>(args, tm_kv, tm_q, tm_rope, n_items, st)
-                 : launch_wide_t<false, 32, false>(args, tm_kv, tm_q, tm_rope, n_items, st);
+    return R == 64   ? launch_wide_t<false, 64, true>(args, tm_kv, tm_q, tm_rope, n_items, st)
+           : R == 32 ? launch_wide_t<false, 32, true>(args, tm_kv, tm_q, tm_rope, n_items, st)
+                     : launch_wide_t<false, 16, true>(args, tm_kv, tm_q, tm_rope, n_items, st);
+  return R == 64   ? launch_wide_t<false, 64, false>(args, tm_kv, tm_q, tm_rope, n_items, st)
+         : R == 32 ? launch_wide_t<false, 32, false>(args, tm_kv, tm_q, tm_rope, n_items, st)
+                   : launch_wide_t<false, 16, false>(args, tm_kv, tm_q, tm_rope, n_items, st);
 }
 
 }  // namespace cpmla

@@ -215,10 +215,12 @@ WORKLOADS = {
     "varlen_p8_h64": dict(varlen=True, n_prefill=8, len_lo=1024, len_hi=65536, n_decode=32,
                           ctx_lo=4096, ctx_hi=131072, H=64, P=8, topk=2048, kv_format="bf16"),
     # smaller cases of the same kernels, for profiler captures (inputs larger
-    # than L2: 1.2 GB of Q, 168 MB of KV; 3.8 GB of Q, 38 MB of KV)
+    # than L2: 1.2 GB of Q, 168 MB of KV; 3.8 GB of Q, 38 MB of KV; 302 MB of
+    # Q, 11 MB of fp8 KV)
     "varlen_p8_h64_s16k": dict(varlen=True, prefill_lens=[9000, 7000], decode_ctx=[40000, 90000],
                                H=64, P=8, topk=2048, kv_format="bf16"),
     "sparse_s12k_h32_p4": dict(S=12288, H=32, P=4, topk=2048, kv_format="bf16"),
+    "sparse_s16k_h16_p2_fp8": dict(S=16384, H=16, P=2, topk=2048, kv_format="fp8"),
 }
 
 
