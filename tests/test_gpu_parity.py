@@ -332,6 +332,33 @@ def test_repeat_runs_bitwise_identical():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("name,kw", [
+    ("sparse_s128k_h16_p2_fp8", dict(S=6000, seed=5)),
+    ("sparse_s32k_h32_p4", dict(S=3000, H=16, seed=31)),
+    ("sparse_s32k_h32_p4", dict(S=3000, seed=22)),
+    ("varlen_p8_h64", dict(prefill_lens=[2500, 1100], decode_ctx=[4100, 9000], seed=24)),
+])
+def test_sparse_repeat_runs_bitwise_identical(name, kw):
+    """The sparse kernel's warps hand shared-memory slots to one another
+    through mbarriers; a missing wait shows up as a run that differs from the
+    others (a few whole tokens, not rounding).  Twelve merged-output runs of
+    each kernel shape (fp8 16 heads, bf16 16 / 32 / 64 heads) must agree bit
+    for bit."""
+    prob = synth.make_problem(name, device="cuda", **kw)
+    plan = cpmla.plan_for(prob, merged=True)
+    kv = cpmla.kv_kwargs(prob)
+    ref = None
+    for _ in range(12):
+        o, lse = plan(prob.q, softmax_scale=prob.scale, sink=prob.sink, idx=prob.idx, **kv)
+        torch.cuda.synchronize()
+        assert cpmla.device_status() == 0
+        if ref is None:
+            ref = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o.view(torch.int16), ref[0].view(torch.int16))
+            assert torch.equal(lse, ref[1])
+
+
 # ----------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name", ["dense_s8192_h16_p2", "sparse_s32k_h32_p4",
                                   "sparse_s128k_h16_p2_fp8", "varlen_p8_h64"])
