@@ -34,6 +34,20 @@ __device__ __forceinline__ uint16_t e4m3x2_rn_sat(float lo, float hi) {
   return d;
 }
 
+// x / b rounded to nearest even in binary32, from y = RN(1/b): q0 = RN(x y)
+// lies within one ulp of x / b, so the remainder x - b q0 is exact in one FMA
+// and RN(q0 + r y) = RN(x / b) -- Markstein's correction step of division by
+// a correctly rounded reciprocal (Markstein 1990; Muller et al., "Handbook of
+// Floating-Point Arithmetic", the FMA-based division chapter).  It holds while
+// b and 1/b are normal and finite; the quotients that fall below the normal
+// range are below 2^-126, where every E4M3 code is a zero, so the codes match
+// those of the exact quotient there too.
+__device__ __forceinline__ float div_by_recip(float x, float b, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, b, x);
+  return __fmaf_rn(r, y, q0);
+}
+
 __device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float *x) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -99,9 +113,18 @@ __global__ void __launch_bounds__(kInsThreads)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));  // within the half-warp
         const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
         uint32_t p[4];
+        if (scale >= 1.17549435e-38f && scale <= 3.40282347e38f) {
+          // one correctly rounded reciprocal per group, three operations a code
+          const float y = __frcp_rn(scale);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          p[i] = e4m3x2_rn_sat(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
+          for (int i = 0; i < 4; ++i)
+            p[i] = e4m3x2_rn_sat(div_by_recip(x[2 * i], scale, y),
+                                 div_by_recip(x[2 * i + 1], scale, y));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            p[i] = e4m3x2_rn_sat(__fdiv_rn(x[2 * i], scale), __fdiv_rn(x[2 * i + 1], scale));
+        }
         codes[k] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
         if ((lane & 15) == 0) cache_scale[su * 4 + 2 * k + (lane >> 4)] = scale;
       }

@@ -276,6 +276,54 @@ def test_kv_cache_insert_fp8_full_size():
     _insert_case(131072, 131072 + 5, 32, 1)
 
 
+def _rounding_boundary_rows(n, seed):
+    """bf16 KV rows whose fp8 quotients x / scale sit on E4M3 rounding
+    midpoints but for the rounding of the scale itself: per 128-channel group
+    the amax A = (32 + u) 2^a has six significant bits (so A / 448 = A / (7 .
+    64) is inexact unless 7 divides 32 + u), and element x = +-3 A 2^(E - 10)
+    gives x / (A / 448) = 21 . 2^(E - 4) = 2^(E) (1 + 5/16), the midpoint
+    between two E4M3 values of that binade; the binary32 quotient lands one
+    ulp to one side of it, so a division off by one ulp flips the code."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((n, 576), np.float32)
+    for t in range(n):
+        for g in range(4):
+            u = int(rng.integers(0, 32))
+            a = int(rng.integers(-24, 24))
+            A = np.float32((32 + u) * 2.0 ** a)
+            grp = np.float32(A) * rng.integers(-31, 32, 128).astype(np.float32) / np.float32(64)
+            grp[0] = A
+            for k in range(1, 40):
+                E = -6 + (k % 15)
+                grp[k] = np.float32((1 if rng.random() < 0.5 else -1) * 3.0 * float(A) * 2.0 ** (E - 10))
+            x[t, 128 * g:128 * (g + 1)] = grp
+        x[t, 512:] = rng.standard_normal(64)
+    kv = torch.from_numpy(x).to(torch.bfloat16)  # the filler rounds; A and the +-3 A 2^(E-10) do not
+    lat = kv[:, :512].float().view(n, 4, 128)
+    want = torch.from_numpy(x[:, :512]).view(n, 4, 128)
+    assert torch.equal(lat[:, :, :40], want[:, :, :40]), "boundary elements not bf16-exact"
+    assert (lat.abs().amax(-1) == want[:, :, 0]).all(), "A is not the group's amax"
+    return kv
+
+
+def test_kv_cache_insert_fp8_rounding_boundaries():
+    """The fp8 insertion's quotients next to E4M3 rounding midpoints: codes
+    and scales bit-exact with the oracle's binary32 division."""
+    n, s_cache = 2048, 2048
+    kv = _rounding_boundary_rows(n, 41)
+    slot = torch.arange(n, dtype=torch.int64)
+    bits = kv.view(torch.int16).numpy().view(np.uint16)
+    want = orc.kv_insert(bits, slot.numpy(), fmt=1, s_cache=s_cache)
+    c8 = torch.zeros((s_cache, 512), dtype=torch.uint8, device="cuda")
+    cs = torch.zeros((s_cache, 4), dtype=torch.float32, device="cuda")
+    cr = torch.zeros((s_cache, 64), dtype=torch.bfloat16, device="cuda")
+    cpmla.mla_kv_cache_insert(kv.cuda(), slot.cuda(), cache_fp8=c8, cache_scale=cs, cache_rope=cr)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    assert np.array_equal(cs.cpu().numpy().view(np.uint32), want["kv_scale"].view(np.uint32))
+    assert np.array_equal(c8.cpu().numpy(), want["kv_fp8"])
+
+
 def test_merge_kernel_against_oracle_merge():
     rng = np.random.default_rng(17)
     n_part, H, T = 300, 6, 120
