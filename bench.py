@@ -19,6 +19,7 @@ partition, host->device copy of the step's inputs, attention, merge, and the
 device->host copy of the output inside the timed region.
 """
 import argparse
+import atexit
 import json
 import os
 import statistics
@@ -78,7 +79,10 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons, every 50 ms from
+    entry (started before the warm-up, since nvidia-smi takes a while to
+    start); `window(t0, t1)` (time.time() seconds) keeps the samples that
+    arrived while the timed steps ran."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -87,12 +91,18 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
 
     def __enter__(self):
+        if self.proc is not None:  # already sampling (started early by clock_sampler)
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -102,9 +112,14 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
+        if self is _SAMPLER:  # the shared sampler runs until the process exits
+            return
+        self.stop()
+
+    def stop(self):
         if self.proc:
             self.proc.terminate()
             try:
@@ -116,7 +131,16 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines, where = self.lines, "whole run"
+        if self.t0 is not None:
+            # a sample is printed shortly after it is taken; a timed region
+            # shorter than the sampling period takes its nearest samples
+            for pad, name in ((0.05, "timed steps"), (0.25, "timed steps +- 0.25 s")):
+                near = [x for x in self.lines if self.t0 - pad + 0.05 <= x[0] <= self.t1 + pad]
+                if near:
+                    lines, where = near, name
+                    break
+        for _, ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -129,9 +153,23 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0, "over": where}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "over": where}
+
+
+_SAMPLER = None
+
+
+def clock_sampler(index):
+    """The process's sampler, started on first use (early, so that samples
+    already flow when a short timed region runs) and stopped at exit."""
+    global _SAMPLER
+    if _SAMPLER is None:
+        _SAMPLER = ClockSampler(index)
+        _SAMPLER.__enter__()
+        atexit.register(_SAMPLER.stop)
+    return _SAMPLER
 
 
 def dist_setup(n_gpus, backend=None):
@@ -232,21 +270,23 @@ def run_kv_insert(args, world, rank, local):
         cpmla.mla_kv_cache_insert(kv_d, slot_d, cache_fp8=c8, cache_scale=cs, cache_rope=cr,
                                   stream=stream)
 
-    for _ in range(args.warmup):
-        flush(1.0)
-        step()
-    torch.cuda.synchronize()
-    assert cpmla.device_status() == 0
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with clock_sampler(local) as clk:
+        for _ in range(args.warmup):
+            flush(1.0)
+            step()
+        torch.cuda.synchronize()
+        assert cpmla.device_status() == 0
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t_clk0 = time.time()
         for i in range(args.steps):
             flush(float(i))
             evs[i][0].record(stream)
             step()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        clk.window(t_clk0, time.time())
     ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, world)
     # end to end: the rows and slots up from pinned memory, the cache rows down
     kv_h, slot_h = kv.pin_memory(), slot.pin_memory()
@@ -353,21 +393,23 @@ def run_topk(args, world, rank, local):
     def step():
         cpmla.mla_topk_select(x, rl, k, out=out, stream=stream)
 
-    for _ in range(args.warmup):
-        flush(1.0)
-        step()
-    torch.cuda.synchronize()
-    assert cpmla.device_status() == 0
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with clock_sampler(local) as clk:
+        for _ in range(args.warmup):
+            flush(1.0)
+            step()
+        torch.cuda.synchronize()
+        assert cpmla.device_status() == 0
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t_clk0 = time.time()
         for i in range(args.steps):
             flush(float(i))
             evs[i][0].record(stream)
             step()
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        clk.window(t_clk0, time.time())
     ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps, world)
     # last step's lists on a few rows against the oracle (outside the timing)
     check_rows = torch.tensor([k, S // 2, S - 1], device=dev)
@@ -499,6 +541,8 @@ def main():
 
     world, rank, local = dist_setup(args.gpus)
     from context_sparse_mla_gb300 import synth
+    if args.impl == "cuda" and torch.cuda.is_available():
+        clock_sampler(local)  # nvidia-smi starts while the inputs are built
 
     if args.workload == KV_INSERT_WORKLOAD:
         run_kv_insert(args, world, rank, local)
@@ -552,11 +596,14 @@ def main():
         barrier(world)
         torch.cuda.synchronize()
         t_wall0 = time.perf_counter()
+        t_clk0 = time.time()
         for i in range(n):
             flush(float(i))  # evict L2 between steps (outside the events)
             step(evs[i], two_launch=two_launch)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall0
+        if clk is not None:
+            clk.window(t_clk0, time.time())
         barrier(world)
         a = [e[0].elapsed_time(e[1]) for e in evs]
         m = [e[1].elapsed_time(e[2]) for e in evs]
@@ -565,8 +612,8 @@ def main():
     # the two-launch path, for the partial-attention and merge kernels' own
     # figures (outside the reported step when the merged path is timed)
     tl_attn, tl_merge, _ = timed(min(args.steps, 20) if merged else 1, True)
-    with ClockSampler(local) as clk:
-        attn_avg, merge_avg, t_wall = timed(args.steps, not merged)
+    with clock_sampler(local) as clk:
+        attn_avg, merge_avg, t_wall = timed(args.steps, not merged, clk)
     if not merged:
         tl_attn, tl_merge = attn_avg, merge_avg
     status = cpmla.device_status()
