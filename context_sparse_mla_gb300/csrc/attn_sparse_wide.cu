@@ -806,16 +806,26 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
     // The sequence: tile j's gathers, then its softmax.  Ring position p
     // reuses the slot of position p - NP, released by the PV GEMM of that
     // tile, which follows that tile's softmax -- done one iteration earlier.
-    // R = 32 and fp8 (five slots): the rope and pair 0 of tile j+1 wait for
-    // nothing and land while the PV GEMM of tile j frees the other slots.
+    // bf16 with five slots (R = 16, 32): the rope and pair 0 of tile j+1
+    // wait for nothing, so they are requested before the softmax of tile j --
+    // the warps would otherwise wait there for the score GEMM's tail, and the
+    // requests queue behind tile j's own -- and only pairs 1-3 of a tile wait
+    // for the PV GEMM of the one before (32 heads: 14.1 ms instead of 14.4).
     // R = 64: the rope goes after pair 1 (the PV GEMM of tile j-1 is done by
-    // then), so the score GEMM's tail only waits for pairs 2 and 3.  fp8:
-    // each pair is converted once its codes have landed, one pair behind the
-    // gathers.
+    // then), so the score GEMM's tail only waits for pairs 2 and 3.  fp8
+    // (five slots too): the rope, then each pair converted once its codes
+    // have landed, one pair behind the gathers; requesting tile j+1's first
+    // units before the softmax made it slower (84.6 ms instead of 80.5).
+    constexpr bool kAhead = !Cfg::kRopeInP && !FP8;
+    if (kAhead && n_tiles > 0) {
+      gather_meta(0);
+      gather_rope(0);
+      gather_pair(0, 0);
+    }
     for (int j = 0; j < n_tiles && ok; ++j) {
-      gather_meta(j);
-      if (!Cfg::kRopeInP) gather_rope(j);
       if (FP8) {
+        gather_meta(j);
+        gather_rope(j);
         gather_pair(j, 0);
         gather_pair(j, 1);
         convert_pair(j, 0);
@@ -824,11 +834,19 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
         gather_pair(j, 3);
         convert_pair(j, 2);
         convert_pair(j, 3);
-      } else {
+      } else if (!kAhead) {
+        gather_meta(j);
         for (int pr = 0; pr < kWPairs; ++pr) {
           gather_pair(j, pr);
-          if (Cfg::kRopeInP && pr == 1) gather_rope(j);
+          if (pr == 1) gather_rope(j);
         }
+      } else {
+        for (int pr = 1; pr < kWPairs; ++pr) gather_pair(j, pr);
+      }
+      if (kAhead && j + 1 < n_tiles) {
+        gather_meta(j + 1);
+        gather_rope(j + 1);
+        gather_pair(j + 1, 0);
       }
       ok = softmax(j);
     }
