@@ -20,16 +20,19 @@
 //     used (the latent is the value, so it stays resident).
 //   * Shared memory: Q [R x 576], P^T [128 keys x R], a ring of NP 32 KB pair
 //     slots (two k-blocks [128 keys x 64 dims]); pair p of tile j at ring
-//     position 4j + p.  R = 16, 32: a rope slot of its own and five pair slots, so
-//     the rope and first pair of tile j+2 are gathered while tile j+1 still
-//     waits for its softmax.  R = 64 (Q alone is 72 KB): four pair slots, and
-//     the rope k-block shares the region of P^T -- the rope of tile j+1 is
-//     gathered once the PV GEMM of tile j has read P^T (after the gathers of
-//     pair 1), and the score GEMM takes it between pairs 1 and 2.
+//     position 4j + p.  R = 16, 32 and fp8: a rope slot of its own and five
+//     pair slots, so the rope and pair 0 of tile j+1 need no slot that tile j
+//     still holds (bf16 requests them before the softmax of tile j).  R = 64
+//     (Q alone is 72 KB): four pair slots, and the rope k-block shares the
+//     region of P^T -- the rope of tile j+1 is gathered once the PV GEMM of
+//     tile j has read P^T (after the gathers of pair 1), and the score GEMM
+//     takes it between pairs 1 and 2.
 //   * Gathers: TMA four-row gathers (tile::gather4, 512 B each) issued by the
-//     16 softmax warps.  One gather takes a warp ~100-200 cycles to issue, so
-//     an SM's gather rate grows with the number of issuing warps (measured:
-//     23 B/clk with 8, 42 with 16, 49 with 20); and a tile's slots are freed
+//     16 softmax warps.  The SM accepts one about every 12-14 cycles and a
+//     gather lands ~1,700 (unloaded) to ~3,000 (loaded) cycles after its
+//     request; a warp's gather instruction stalls it until the SM has
+//     accepted it, so 16 issuing warps keep the queue full (measured: 23
+//     B/clk with 8 warps, 42 with 16, 49 with 20).  A tile's slots are freed
 //     by the PV GEMM that follows its softmax, so the softmax warps are idle
 //     exactly when the next tile's gathers are due.  Warp w of the 16 fills
 //     keys 16 (w % 8) .. +15 of k-block w / 8 of every pair slot, and keys
@@ -41,8 +44,8 @@
 //   * Softmax: four warpgroups (warps 4-7, 8-11, 12-15, 16-19) take R/4 score
 //     columns each; thread i = TMEM lane i = key i of the tile (dv i of an O^T
 //     chunk).  Base 2, with a row reference moved only when a score passes it
-//     by 2^8.  Per tile the warps run the softmax first, then the gathers it
-//     unblocks.
+//     by 2^8.  Per tile the warps run the gathers of tile j (those the
+//     previous softmax unblocked), then its softmax.
 //   * fp8 (R = 16, five pair slots, a rope slot of its own): gather warp w
 //     fetches the raw E4M3 codes of keys 8 w .. 8 w + 7 of a pair (128 bytes a
 //     key, unswizzled, into the upper half of the slot) and, once they have
