@@ -43,8 +43,8 @@ NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
                      # 16002-token capture of the same shape (1.432 + 1.018 GB),
                      # scaled to the workload's 326209 tokens
                      ("varlen_p8_h64", "merged"): int(2.450296e9 * 326209 / 16002),
-                     # 12288-token capture (586.2 + 375.6 MB), scaled to 32768 tokens
-                     ("sparse_s32k_h32_p4", "merged"): int(961.832448e6 * 32768 / 12288),
+                     # 12288-token capture (586.4 + 376.7 MB), scaled to 32768 tokens
+                     ("sparse_s32k_h32_p4", "merged"): int(963.121664e6 * 32768 / 12288),
                      # 16384-token capture (455.4 + 245.2 MB), scaled to 131072 tokens
                      ("sparse_s128k_h16_p2_fp8", "merged"): int(700.634368e6 * 131072 / 16384)}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
