@@ -60,6 +60,9 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
                   "%s: unknown kv_format %d", fn, kv_format);
   if (!sparse && kv_format != CPMLA_KV_BF16)
     return fail(CPMLA_ERR_UNSUPPORTED, "%s: dense attention takes CPMLA_KV_BF16 only", fn);
+  if (sparse && kv_format == CPMLA_KV_FP8_E4M3_G128 && H > 16 && H % 16 != 0)
+    return fail(CPMLA_ERR_UNSUPPORTED,
+                "%s: H=%d over the fp8 cache must be at most 16 or a multiple of 16", fn, H);
   CPMLA_CHECK_ARG(std::isfinite(softmax_scale) && softmax_scale > 0.f, "%s: bad softmax_scale",
                   fn);
   CPMLA_CHECK_ARG(q_token_stride >= (int64_t)H * CPMLA_DQK && q_token_stride % 8 == 0,

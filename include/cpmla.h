@@ -199,7 +199,10 @@ int pcp_gather_rows_f32(const float *src, int64_t src_row_stride, int64_t n_src,
  *   q            bf16 [T, H, 576]; token g's head h starts at
  *                q + g*q_token_stride + h*576 (elements); 16-byte aligned
  *   q_token_stride  elements between tokens, >= H*576, multiple of 8 (host)
- *   H            heads, 1..128; if H > 64 it must be a multiple of 64 (host)
+ *   H            heads, 1..128; if H > 64 it must be a multiple of 64; sparse
+ *                over the fp8 cache: at most 16, or a multiple of 16 (a CTA
+ *                takes 16 heads of a token); otherwise CPMLA_ERR_UNSUPPORTED
+ *                (host)
  *   kv_format    CPMLA_KV_* (host).  Dense accepts CPMLA_KV_BF16 only.
  *   kv / kv_fp8, kv_scale, kv_rope   per kv_format (unused ones may be NULL);
  *                each 16-byte aligned

@@ -116,6 +116,14 @@ def test_attention_argument_checks_fail_before_the_device(lib):
     rc = lib.mla_partial_attn_sparse(None, 576, 1, 0, None, None, None, None, 16, None, None, None,
                                      None, 1, None, None, None, 0, 0.07, None, None, None)
     assert rc == cpmla.CPMLA_ERR_ARG  # k = 0
+    # sparse over the fp8 cache takes 16 heads a CTA: H = 24 is refused, 48 passes this check
+    rc = lib.mla_partial_attn_sparse(None, 576 * 24, 24, 1, None, None, None, None, 16, None, None,
+                                     None, None, 1, None, None, None, 8, 0.07, None, None, None)
+    assert rc == cpmla.CPMLA_ERR_UNSUPPORTED
+    assert b"H=24" in lib.cpmla_last_error()
+    rc = lib.mla_partial_attn_sparse(None, 576 * 48, 48, 1, None, None, None, None, 16, None, None,
+                                     None, None, 1, None, None, None, 8, 0.07, None, None, None)
+    assert rc == cpmla.CPMLA_ERR_ARG  # past the head check: NULL pointers
 
 
 def test_merged_attention_argument_checks(lib):
