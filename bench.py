@@ -328,7 +328,8 @@ def run_kv_insert(args, world, rank, local):
            "config": cfg,
            "roofline": {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": pk["hbm"],
                         "unit": "GB/s", "frac": round(gbs / world / pk["hbm"], 4),
-                        "traffic": None, "kernel": "kv_insert_kernel",
+                        # DRAM read + write of one launch of this workload (ncu)
+                        "traffic": 152071168 + 52147968, "kernel": "kv_insert_kernel",
                         "peak_source": pk["source"] + " HBM copy"},
            "e2e": {"value": round(world * bytes_step / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                    "ms_per_step": round(e2e_ms, 3),

@@ -12,7 +12,7 @@
 // even, saturating at +-448.
 //
 // HBM-bound: per token 1152 B read, 576 x 2 B (bf16) or 512 + 16 + 128 B
-// (fp8) written.  A warp takes four tokens at a time, all their loads in
+// (fp8) written.  A warp takes two tokens at a time, all their loads in
 // flight before the first store; per token, lane l moves latent 16-byte
 // chunks l and l + 32 (each warp access one contiguous 512 B span), lanes 0-7
 // the rope; the 16 chunks of a 128-channel group sit in one half-warp, whose
@@ -57,7 +57,11 @@ __device__ __forceinline__ void bf16x8_to_float(const uint4 &v, float *x) {
   }
 }
 
-constexpr int kTokPerWarp = 4;  // tokens whose loads a warp has in flight at once
+// tokens whose loads a warp has in flight at once: two, with one pass of
+// 128-thread blocks over the tokens (measured on the 131072-token insertion:
+// 0.0452 ms at two, 0.0503 at four, 0.0514 at one; 256-thread blocks and
+// grids capped at 8-16 blocks per SM were slower)
+constexpr int kTokPerWarp = 2;
 
 __global__ void __launch_bounds__(kInsThreads)
     kv_insert_kernel(const __nv_bfloat16 *__restrict__ kv, int64_t kv_stride, int n,
