@@ -38,7 +38,7 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 163_316_480 + 96_105_472,
+NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 162_849_280 + 96_004_864,
                      ("topk_s8k_k2048", "topk"): 126_366_464 + 11_335_424,
                      # 16002-token capture of the same shape (1.432 + 1.018 GB),
                      # scaled to the workload's 326209 tokens

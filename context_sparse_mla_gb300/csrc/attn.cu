@@ -213,7 +213,25 @@ int attn_entry(bool sparse, const void *q, int64_t q_token_stride, int H, int kv
   const CUresult cr = encode(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kv, CPMLA_DQK, 2, kKbDims,
                              kTileKeys, CU_TENSOR_MAP_SWIZZLE_128B);
   if (cr != CUDA_SUCCESS) return fail(CPMLA_ERR_CUDA, "%s: tensor map encode failed (%d)", fn, (int)cr);
-  return launch_dense(args, tm, (int)n_items, st);
+  // Q as for the sparse kernel, in boxes of 64 dims x hc heads x 1 token (the
+  // kernel uses it when hc is a multiple of 8)
+  CUtensorMap tm_q;
+  memset(&tm_q, 0, sizeof tm_q);
+  {
+    const int64_t T_q = (int64_t)(merged ? T : 0);
+    cuuint64_t qdims[3] = {(cuuint64_t)CPMLA_DQK, (cuuint64_t)H,
+                           (cuuint64_t)(T_q > 0 ? T_q : INT32_MAX)};
+    cuuint64_t qstr[2] = {(cuuint64_t)CPMLA_DQK * 2, (cuuint64_t)q_token_stride * 2};
+    cuuint32_t qbox[3] = {(cuuint32_t)kKbDims, (cuuint32_t)args.hc, 1};
+    cuuint32_t qes[3] = {1, 1, 1};
+    const CUresult cq = enc(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), qdims,
+                            qstr, qbox, qes, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cq != CUDA_SUCCESS)
+      return fail(CPMLA_ERR_CUDA, "%s: Q tensor map encode failed (%d)", fn, (int)cq);
+  }
+  return launch_dense(args, tm, tm_q, (int)n_items, st);
 }
 
 }  // namespace cpmla

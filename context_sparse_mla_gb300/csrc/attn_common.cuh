@@ -194,7 +194,10 @@ int launch_merge_to_tokens(const float *o_part, const float *lse_part, int64_t n
                            const int32_t *out_tok, int T_out, int *status, cudaStream_t st);
 
 // Launchers (one per translation unit); n_items CTAs, one work item each.
-int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st);
+// Dense: tm_q = Q as [T, H, 576] in boxes of 64 dims x hc heads x 1 token
+// (used when hc is a multiple of 8).
+int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &tm_q,
+                 int n_items, cudaStream_t st);
 // Sparse (attn_sparse_wide.cu): bf16 KV with R = 16, 32 or 64 heads per CTA,
 // or fp8 KV with R = 16.  One-row gather maps: bf16: tm_kv = tm_rope = the
 // KV (box 64 x 1, 128-byte swizzle); fp8: tm_kv = the E4M3 codes (box 128 x

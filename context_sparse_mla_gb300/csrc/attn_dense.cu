@@ -63,6 +63,7 @@ struct DenseCtrl {
   uint64_t p_free;
   uint64_t o_full;
   uint64_t drain[2];
+  uint64_t q_full;  // Q rows landed (TMA path)
   uint32_t tmem_base;
   int abort;
   int n_tiles;
@@ -76,8 +77,9 @@ struct DenseCtrl {
   float m_ref[kR];
   float alpha[kR];
   float lse[kR];
-  float inv_l[kR];
-  float sfac[kR];  // merged output: sink factor per row
+  alignas(16) float inv_l[kR];
+  alignas(16) float sfac[kR];  // merged output: sink factor per row
+  int64_t obase[kR];  // partial output: element offset of a row in o_part, -1: none
   int gtok[kR];    // merged output: global token a row writes, or -1
   int64_t tlo[kR], thi[kR];  // per token of the item: valid keys (global rows, inclusive)
   int ttok[kR];              // per token: global token, -1 past the last shard row
@@ -129,7 +131,8 @@ __device__ __forceinline__ uint32_t ring_pos_v(int j, int ch, int n) {
 // (AttnArgs::o_out) instead of the partial (o_part / lse_part).
 template <bool MERGED>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_dense_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv) {
+    mla_dense_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tm_kv,
+                     const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *sQ = smem;                      // 9 k-blocks of [64 rows x 64 dims]
@@ -164,12 +167,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&c.o_full, 1);
     mbar_init(&c.drain[0], 1);
     mbar_init(&c.drain[1], 1);
+    mbar_init(&c.q_full, 1);
     c.abort = 0;
     c.need_rescale[0] = c.need_rescale[1] = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&c.tmem_base, kTmemCols);
   if (warp >= 2 && warp < 2 + kProducers && lane == 0) tma_prefetch_desc(&tm_kv);
+  if (warp == 1 && lane == 0) tma_prefetch_desc(&tm_q);
   if (tid < kR) {
     c.m_ref[tid] = -INFINITY;
     c.alpha[tid] = 1.f;
@@ -206,9 +211,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.town[tid] = own;
   }
   __syncthreads();
-  // Q rows -> K-major, 128-byte-swizzled k-blocks (zero rows for padding):
-  // every thread issues all its loads before its first store
-  {
+  // Q rows -> K-major, 128-byte-swizzled k-blocks (zero rows for padding).
+  // When an item's tokens start on whole 1 KB swizzle atoms (hc a multiple of
+  // 8), each token's hc heads come by TMA, nine boxes of 64 dims landing on
+  // q_full, issued once the prologue is done by the first lanes of the eight
+  // softmax warps (idle until the first scores; one thread's TMA issues take a
+  // few hundred cycles each), while the producers already request the first
+  // K tiles; the rows of absent tokens and the padding rows are zeroed by
+  // their own thread below.  Otherwise every thread issues all its loads
+  // before its first store.
+  const bool q_tma = (a.hc & 7) == 0;
+  if (q_tma) {
+    if (tid == 0) {
+      uint32_t bytes = 0;
+      for (int l = 0; l < a.g && l * a.hc < r_valid; ++l)
+        if (c.ttok[l] >= 0) bytes += (uint32_t)(kKb * a.hc * 128);
+      mbar_arrive_expect_tx(&c.q_full, bytes);
+    }
+  } else {
     constexpr int kPer = kR * (CPMLA_DQK / 8) / kThreads;  // 12 16-byte chunks per thread
     static_assert(kPer * kThreads == kR * (CPMLA_DQK / 8), "Q chunks per thread");
     uint4 v[kPer];
@@ -275,6 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     c.rlo[tid] = rlo;
     c.rhi[tid] = rhi;
     c.gtok[tid] = gt;
+    // TMA path: a row that no copy fills (padding, absent token) is zero
+    if (q_tma && (tid >= r_valid || c.ttok[l] < 0)) {
+#pragma unroll 1
+      for (int kb = 0; kb < kKb; ++kb)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4 *>(sQ + kb * (kR * 128) + tid * 128 + ch * 16) =
+              make_uint4(0, 0, 0, 0);
+    }
   }
   fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
   tc_fence_before();
@@ -285,6 +314,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tO = tmem + 2 * kR;  // O^T chunk c at tO + c*64; S^T buffer b at tmem + b*64
   volatile int *abort = &c.abort;
 
+  // Q copies of the TMA path: box (token l, k-block kb) = number b = 9 l + kb,
+  // issued by the first lane of softmax warp b % 8
+  if (q_tma && warp >= kSoftmaxWarp0 && lane == 0) {
+    const int who = warp - kSoftmaxWarp0;
+    for (int b = who; b < kKb * a.g; b += 8) {
+      const int l = b / kKb, kb = b - l * kKb;
+      if (l * a.hc >= r_valid || c.ttok[l] < 0) continue;
+      tma_load_3d(sQ + kb * (kR * 128) + l * a.hc * 128, &tm_q, kb * kKbDims, h0, c.ttok[l],
+                  &c.q_full);
+    }
+  }
+
   if (warp == 0) {
     // ---------------------------------------------------- score-GEMM issuer
     // takes the K items of the ring sequence
@@ -292,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_qk = idesc_bf16(128, kR, 0, 0);
       const uint64_t dq0 = smem_desc(smem_u32(sQ), 16, 1024, kSwz128);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), 16, 1024, kSwz128);
-      bool ok = true;
+      bool ok = !q_tma || n_tiles == 0 || mbar_wait(&c.q_full, 0, abort, a.status);
       for (int i = 0; i < n_tiles && ok; ++i) {
         const int sb = i & 1;
         if (i >= 2 && !mbar_wait(&c.s_free[sb], ((i >> 1) - 1) & 1, abort, a.status)) {
@@ -328,6 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&c.drain[0]);
         drain_wait(&c.drain[0], 0);
       }
+      // the Q copies have landed before the CTA can exit
+      if (q_tma) drain_wait(&c.q_full, 0);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -532,18 +575,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool empty = !(l > 0.f) || m == -INFINITY;
         c.lse[r] = empty ? -INFINITY : (m + __log2f(l)) * 0.69314718055994530942f;
         c.inv_l[r] = empty ? 0.f : 1.f / l;
+        float sf = 1.f;
+        int64_t ob = -1;
         if (r < r_valid) {
           const int lrow = r / a.hc, hh = r - lrow * a.hc;
           const int i = row0 + lrow;
           if (!MERGED) {
-            if (i < a.n_rows) a.lse_part[(int64_t)i * a.H + h0 + hh] = c.lse[r];
+            if (i < a.n_rows) {
+              a.lse_part[(int64_t)i * a.H + h0 + hh] = c.lse[r];
+              ob = ((int64_t)i * a.H + h0 + hh) * CPMLA_DV;
+            }
           } else if (c.gtok[r] >= 0) {
-            c.sfac[r] = sink_factor(a.sink, h0 + hh, c.lse[r]);
+            sf = sink_factor(a.sink, h0 + hh, c.lse[r]);
             a.lse_out[(int64_t)c.gtok[r] * a.H + h0 + hh] = c.lse[r];
           }
         }
+        c.sfac[r] = sf;
+        c.obase[r] = ob;
       }
       named_bar_sync(bar_id, 128);
+      // thread t owns dv t of each O^T chunk; a row's 1/l and sink factor are
+      // read once per block of 16 rows (four-wide broadcasts)
+      const bool odd = (lane & 1) != 0;
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
 #pragma unroll
@@ -556,21 +609,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int x = 0; x < 16; ++x) o[x] = 0.f;
           }
+          float inv[16], sfb[16];
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int r = cbase + cc * 16 + x;
-            if (r < r_valid) {
-              const int lrow = r / a.hc, hh = r - lrow * a.hc;
-              const int i = row0 + lrow;
-              if (!MERGED) {
-                if (i < a.n_rows)
-                  a.o_part[((int64_t)i * a.H + h0 + hh) * CPMLA_DV + ch * 128 + t] =
-                      o[x] * c.inv_l[r];
-              } else if (c.gtok[r] >= 0) {
-                // merged: stage bf16 rows [row][dv] in the idle ring, stored below
-                reinterpret_cast<__nv_bfloat16 *>(sRing)[r * CPMLA_DV + ch * 128 + t] =
-                    __float2bfloat16_rn((o[x] * c.inv_l[r]) * c.sfac[r]);
-              }
+          for (int x = 0; x < 16; x += 4) {
+            const float4 i4 = *reinterpret_cast<const float4 *>(&c.inv_l[cbase + cc * 16 + x]);
+            inv[x] = i4.x;
+            inv[x + 1] = i4.y;
+            inv[x + 2] = i4.z;
+            inv[x + 3] = i4.w;
+            if (MERGED) {
+              const float4 s4 = *reinterpret_cast<const float4 *>(&c.sfac[cbase + cc * 16 + x]);
+              sfb[x] = s4.x;
+              sfb[x + 1] = s4.y;
+              sfb[x + 2] = s4.z;
+              sfb[x + 3] = s4.w;
+            }
+          }
+          if (!MERGED) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+              const int64_t ob = c.obase[cbase + cc * 16 + x];
+              if (ob >= 0) a.o_part[ob + ch * 128 + t] = o[x] * inv[x];
+            }
+          } else {
+            // merged: bf16 rows [row][dv] staged in the idle ring (every row:
+            // the bulk copies below take only the owned tokens' rows); lane
+            // pairs trade one value so that the even lane stores row r at dv
+            // t, t+1 and the odd lane row r+1 at dv t-1, t
+#pragma unroll
+            for (int x = 0; x < 16; x += 2) {
+              const int r = cbase + cc * 16 + x;
+              // (o / l) x sink factor, rounded as the merge kernel rounds it
+              const float v0 = (o[x] * inv[x]) * sfb[x];
+              const float v1 = (o[x + 1] * inv[x + 1]) * sfb[x + 1];
+              const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+              const uint32_t w = odd ? pack_bf16x2(got, v1) : pack_bf16x2(v0, got);
+              // (writing these pairs straight to o_out instead measured 1.416
+              // ms against 1.393 for the staged rows and bulk copies)
+              *reinterpret_cast<uint32_t *>(sRing + ((size_t)(odd ? r + 1 : r) * CPMLA_DV +
+                                                     ch * 128 + (t & ~1)) * 2) = w;
             }
           }
         }
@@ -607,11 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, int n_items, cudaStream_t st) {
+int launch_dense(const AttnArgs &args, const CUtensorMap &tm_kv, const CUtensorMap &tm_q,
+                 int n_items, cudaStream_t st) {
   auto kern = args.o_out ? mla_dense_kernel<true> : mla_dense_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return cuda_fail(e, "dense attention: set shared memory size");
-  kern<<<n_items, kThreads, kSmem, st>>>(args, tm_kv);
+  kern<<<n_items, kThreads, kSmem, st>>>(args, tm_kv, tm_q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "dense attention: launch");
   return CPMLA_OK;
