@@ -134,8 +134,8 @@ struct WideCtrl {
   alignas(16) float m_ref[R];
   alignas(16) float alpha[R];
   float lse[R];
-  float inv_l[R];
-  float sfac[R];  // merged output: sink factor per head
+  alignas(16) float inv_l[R];
+  alignas(16) float sfac[R];  // merged output: sink factor per head
 };
 
 template <bool FP8, int R>
@@ -256,14 +256,11 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
   if (!FP8) {
     // Q rows of this item: nine TMA boxes [R heads x 64 dims] straight into
     // the MMA's K-major, 128-byte-swizzled k-blocks (heads past H read as
-    // zero); they land while the list is scanned and the first keys are
-    // gathered
-    if (tid == 0 && row_ok) {
-      mbar_arrive_expect_tx(&c.q_full, (uint32_t)(kKb * R * 128));
-#pragma unroll 1
-      for (int kb = 0; kb < kKb; ++kb)
-        tma_load_3d(sQ + kb * (R * 128), &tm_q, kb * kKbDims, h0, (int)gq, &c.q_full);
-    }
+    // zero), landing on q_full while the first keys are gathered.  Armed
+    // here; the two PV-issuing threads issue the copies once the prologue is
+    // done (a thread's TMA issues take a few hundred cycles each, which the
+    // prologue would otherwise wait for)
+    if (tid == 0 && row_ok) mbar_arrive_expect_tx(&c.q_full, (uint32_t)(kKb * R * 128));
   } else {
     // fp8: Q rows by the threads, the latent part converted to fp16 (it
     // meets fp16 codes in the MMA; the rope part stays bf16 against the bf16
@@ -284,6 +281,24 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
       *reinterpret_cast<uint4 *>(sQ + kb * (R * 128) + r * 128 + ((cc ^ (r & 7)) << 4)) = w;
     }
     fence_proxy_async_smem();  // Q written by threads, read by tcgen05.mma
+  }
+  // the key-row warp's row constants and the list entries of tile 0, loaded
+  // beside the scan below instead of after the prologue
+  int mw_tpos = 0, mw_lo = 0, mw_hi = 0, mw_len = 0;
+  int64_t mw_base = 0;
+  const int32_t *mw_lst = nullptr;
+  int mw_nxt[4] = {-1, -1, -1, -1};
+  if (warp == kWMetaWarp && row_ok) {
+    mw_tpos = a.pos[row];
+    mw_base = a.kv_start[a.req[row]];
+    mw_lst = topk_window(a, row, gq, &mw_len);
+    mw_lo = a.kv_lo ? a.kv_lo[row] : 0;
+    mw_hi = a.kv_hi ? (a.kv_hi[row] < mw_tpos ? a.kv_hi[row] : mw_tpos) : mw_tpos;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = q * 32 + lane;
+      mw_nxt[q] = e < mw_len ? __ldg(mw_lst + e) : -1;
+    }
   }
   {
     // the last non-empty slot of the row's list: every thread scans its
@@ -397,6 +412,12 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
       const uint64_t dp0 = smem_desc(smem_u32(sP), 8192, 8 * PLayout<R>::row_bytes,
                                      PLayout<R>::swz);
       const uint64_t dr0 = smem_desc(smem_u32(sRing), kKbBytes, 1024, kSwz128);
+      if (!FP8 && row_ok && me < 2) {
+        // bf16: Q's nine boxes, k-blocks me, me + 2, ...
+#pragma unroll 1
+        for (int kb = me; kb < kKb; kb += 2)
+          tma_load_3d(sQ + kb * (R * 128), &tm_q, kb * kKbDims, h0, (int)gq, &c.q_full);
+      }
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
         if (!mbar_wait(&c.p_full, j & 1, abort, a.status)) {
@@ -437,18 +458,14 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
     // the row's range (fp8: and its four scales); the list entries of tile
     // j+1 load while tile j's are resolved
     if (row_ok && n_tiles > 0) {
-      const int tpos = a.pos[row];
-      const int64_t base = a.kv_start[a.req[row]];
-      int len = 0;
-      const int32_t *lst = topk_window(a, row, gq, &len);
-      const int lo = a.kv_lo ? a.kv_lo[row] : 0;
-      const int hi = a.kv_hi ? (a.kv_hi[row] < tpos ? a.kv_hi[row] : tpos) : tpos;
+      const int tpos = mw_tpos;
+      const int64_t base = mw_base;
+      const int len = mw_len;
+      const int32_t *lst = mw_lst;
+      const int lo = mw_lo, hi = mw_hi;
       int nxt[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int e = q * 32 + lane;
-        nxt[q] = e < len ? __ldg(lst + e) : -1;
-      }
+      for (int q = 0; q < 4; ++q) nxt[q] = mw_nxt[q];
       for (int j = 0; j < n_tiles; ++j) {
         int cur[4];
 #pragma unroll
@@ -885,6 +902,21 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
         }
       }
       named_bar_sync(bar_id, 128);
+      // this group's 1/l and sink factors, read once (four-wide broadcasts)
+      float inv[RC], sf[RC];
+#pragma unroll
+      for (int y = 0; y < RC; y += 4) {
+        const float4 i4 = *reinterpret_cast<const float4 *>(&c.inv_l[cbase + y]);
+        inv[y] = i4.x;
+        inv[y + 1] = i4.y;
+        inv[y + 2] = i4.z;
+        inv[y + 3] = i4.w;
+        const float4 s4 = *reinterpret_cast<const float4 *>(&c.sfac[cbase + y]);
+        sf[y] = s4.x;
+        sf[y + 1] = s4.y;
+        sf[y + 2] = s4.z;
+        sf[y + 3] = s4.w;
+      }
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         float o[RC];
@@ -899,7 +931,7 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
           for (int y = 0; y < RC; ++y) {
             const int r = cbase + y;
             if (r >= r_valid || !row_ok) continue;
-            a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] = o[y] * c.inv_l[r];
+            a.o_part[((int64_t)row * a.H + h0 + r) * CPMLA_DV + ch * 128 + t] = o[y] * inv[y];
           }
         } else {
           // merged: bf16 pairs of neighbouring dv -- lane pairs trade one
@@ -911,8 +943,8 @@ __global__ void __launch_bounds__(WideCfg<FP8, R>::kThreads, 1)
 #pragma unroll
           for (int y = 0; y < RC; y += 2) {
             const int r = cbase + y;
-            const float v0 = r < r_valid ? (o[y] * c.inv_l[r]) * c.sfac[r] : 0.f;
-            const float v1 = r + 1 < r_valid ? (o[y + 1] * c.inv_l[r + 1]) * c.sfac[r + 1] : 0.f;
+            const float v0 = r < r_valid ? (o[y] * inv[y]) * sf[y] : 0.f;
+            const float v1 = r + 1 < r_valid ? (o[y + 1] * inv[y + 1]) * sf[y + 1] : 0.f;
             const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
             const int hr = odd ? r + 1 : r;
             if (own && hr < r_valid) {
