@@ -407,6 +407,28 @@ def test_sparse_repeat_runs_bitwise_identical(name, kw):
             assert torch.equal(lse, ref[1])
 
 
+@pytest.mark.parametrize("merged", [False, True])
+def test_dense_repeat_runs_bitwise_identical(merged):
+    """The dense kernel's warps hand ring slots, S^T buffers, P^T and O^T to
+    one another through mbarriers; a phase passed one use early shows up as a
+    run that differs from the others (whole rows, not rounding).  Twelve runs
+    of 750 work items (several waves of CTAs) must agree bit for bit, with the
+    two-launch path and with the merged epilogue."""
+    prob = synth.make_problem("dense_s8192_h16_p2", S=3000, device="cuda", seed=27)
+    plan = cpmla.plan_for(prob, merged=merged)
+    kv = cpmla.kv_kwargs(prob)
+    ref = None
+    for _ in range(12):
+        o, lse = plan(prob.q, softmax_scale=prob.scale, sink=prob.sink, idx=prob.idx, **kv)
+        torch.cuda.synchronize()
+        assert cpmla.device_status() == 0
+        if ref is None:
+            ref = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o.view(torch.int16), ref[0].view(torch.int16))
+            assert torch.equal(lse, ref[1])
+
+
 # ----------------------------------------------------- full-size workloads
 @pytest.mark.parametrize("name", ["dense_s8192_h16_p2", "sparse_s32k_h32_p4",
                                   "sparse_s128k_h16_p2_fp8", "varlen_p8_h64"])
