@@ -38,15 +38,15 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
-NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 162_849_280 + 96_004_864,
+NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 162_865_408 + 95_957_760,
                      ("topk_s8k_k2048", "topk"): 126_366_464 + 11_335_424,
-                     # 16002-token capture of the same shape (1.432 + 1.018 GB),
+                     # 16002-token capture of the same shape (1.433 + 1.018 GB),
                      # scaled to the workload's 326209 tokens
-                     ("varlen_p8_h64", "merged"): int(2.450296e9 * 326209 / 16002),
-                     # 12288-token capture (586.4 + 376.7 MB), scaled to 32768 tokens
-                     ("sparse_s32k_h32_p4", "merged"): int(963.121664e6 * 32768 / 12288),
-                     # 16384-token capture (455.4 + 245.2 MB), scaled to 131072 tokens
-                     ("sparse_s128k_h16_p2_fp8", "merged"): int(700.634368e6 * 131072 / 16384)}
+                     ("varlen_p8_h64", "merged"): int((1.432820e9 + 1.018263e9) * 326209 / 16002),
+                     # 12288-token capture (587.7 + 376.8 MB), scaled to 32768 tokens
+                     ("sparse_s32k_h32_p4", "merged"): int((587.681280e6 + 376.763136e6) * 32768 / 12288),
+                     # 16384-token capture (451.9 + 244.5 MB), scaled to 131072 tokens
+                     ("sparse_s128k_h16_p2_fp8", "merged"): int((451.890176e6 + 244.510464e6) * 131072 / 16384)}
 FLOPS_PER_KEY_HEAD = 2 * 576 + 2 * 512
 L2_FLUSH_BYTES = 512 << 20
 
