@@ -13,10 +13,15 @@
 // bulk L2 prefetch of a CTA's next row is issued as soon as its current row
 // has been filtered, so HBM streams while the selection runs on chip.  Per
 // row:
-//   1. sample: 256 groups of 8 consecutive logits spread over the row; the
-//      threshold c is the sample's r-th largest, r chosen so that about
-//      k + 3 standard deviations of the row are expected at or above it;
-//      rows of at most C logits skip this (c = -inf).
+//   1. threshold c: extrapolated from the CTA's previous row (its threshold,
+//      the candidates that kept and its k-th largest value give the count of
+//      the tail as a function of the threshold; the count scales with the
+//      row's length), aiming at k + 4 sqrt(k) candidates; or, for a CTA's
+//      first row, when the extrapolation reaches too far, or when its count
+//      misses, a sample: 256 groups of 8 consecutive logits spread over the
+//      row, c its r-th largest, r chosen so that about k + 3 standard
+//      deviations of the row are expected at or above it.  Rows of at most C
+//      logits skip this (c = -inf).
 //   2. filter: one coalesced pass keeps every logit >= c, with its column,
 //      as a candidate in shared memory (warp-aggregated appends).
 //   3. exact selection over the candidates when there are between k and C of
@@ -26,9 +31,10 @@
 //   4. a bitmap over the row's columns marks the keys above tau and, cut in
 //      column order, the ties; a scan of its words writes the k columns in
 //      ascending order.
-// When the sample's threshold fails (fewer than k or more than C logits at or
-// above it), steps 3-4 run over the row in global memory instead: slower,
-// the same result.
+// An extrapolated threshold that fails the count (fewer than k or more than C
+// logits at or above it) is replaced by the sample's, and the row filtered
+// again; when the sample's fails too, steps 3-4 run over the row in global
+// memory instead: slower, the same result.
 #include <algorithm>
 #include <cmath>
 
@@ -50,6 +56,11 @@ constexpr int kPrefetchChunk = 32768;
 // flight per thread): 1.279 ms on the 32768-row case against 1.302 with four
 // (2k + 1024, four loads); five and eight were no faster.
 constexpr int kTkMinBlocks = 6;
+// A row's threshold is extrapolated from the CTA's previous row when it lies
+// within this many times the previous row's (c, tau) span of counts (2, 4, 8,
+// 16 spans: 1.121, 1.100, 1.095, 1.095 ms on the 32768-row case; the sampled
+// threshold alone 1.279 ms).
+constexpr int kExtrapSpans = 8;
 
 static_assert(kSample == 8 * kTkThreads, "one sample group of 8 logits per thread");
 static_assert(kBins == kTkThreads, "one histogram bin per thread when clearing");
@@ -96,6 +107,16 @@ struct Selection {
   uint32_t tau;  // key of the kth-largest element
   int n_gt;      // elements with key > tau (< kth)
   int n_eq;      // elements with key == tau (n_gt + n_eq >= kth)
+};
+
+// A CTA's last filtered row (every thread holds the same copy): the threshold
+// c its filter used, the candidates that kept (cnt, of a row of n logits) and
+// the row's kth-largest value tau.  c and tau are two points of the row's
+// upper tail, from which the next row's threshold is extrapolated.
+struct TkPrev {
+  float c, tau;
+  int cnt, n;
+  bool ok;
 };
 
 // Inclusive scan of one int per thread over the block.
@@ -321,7 +342,7 @@ __device__ void emit_selection(const Elem &elem, int count, const Selection &s, 
 __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, int k, int cap,
                                            int32_t *__restrict__ orow, uint32_t *ckey,
                                            int32_t *ccol, uint32_t *bm, TkScratch &sc,
-                                           const float *next_x, int next_n) {
+                                           const float *next_x, int next_n, TkPrev &prev) {
   const int tid = threadIdx.x, lane = tid & 31;
   const float4 *x4 = reinterpret_cast<const float4 *>(x);
   const int nw = (n + 31) >> 5;
@@ -329,31 +350,52 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
 
   bool try_candidates = cap >= k;
   float c = -INFINITY;
-  if (try_candidates && n > cap) {
-    if (n >= kSample) {
-      // 1. the sample: group tid at a float4 boundary, 8 logits, inside the row
-      const int64_t off = ((int64_t)tid * (n - 8) / (kTkThreads - 1)) & ~(int64_t)3;
-      const float4 a = __ldg(x4 + off / 4), b = __ldg(x4 + off / 4 + 1);
-      const uint32_t sk[8] = {order_key(a.x), order_key(a.y), order_key(a.z), order_key(a.w),
-                              order_key(b.x), order_key(b.y), order_key(b.z), order_key(b.w)};
-      uint32_t lo = sk[0], hi = sk[0];
+  // 1. the sample: group tid at a float4 boundary, 8 logits, inside the row;
+  // c = the sample's r-th largest, r chosen so that about k + 3 standard
+  // deviations of the row are expected at or above it
+  auto sample_threshold = [&]() -> float {
+    const int64_t off = ((int64_t)tid * (n - 8) / (kTkThreads - 1)) & ~(int64_t)3;
+    const float4 a = __ldg(x4 + off / 4), b = __ldg(x4 + off / 4 + 1);
+    const uint32_t sk[8] = {order_key(a.x), order_key(a.y), order_key(a.z), order_key(a.w),
+                            order_key(b.x), order_key(b.y), order_key(b.z), order_key(b.w)};
+    uint32_t lo = sk[0], hi = sk[0];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        ckey[j * kTkThreads + tid] = sk[j];  // (the select ignores the order)
-        lo = min(lo, sk[j]);
-        hi = max(hi, sk[j]);
-      }
-      const float p = (float)k / (float)n;
-      const float want = (float)kSample * p + 3.f * sqrtf((float)kSample * p * (1.f - p)) + 2.f;
-      const int r = min(kSample, max(1, (int)ceilf(want)));
-      const Selection s = block_select([&](int i) { return ckey[i]; }, kSample, r, lo, hi, sc);
-      c = key_value(s.tau);
-    } else {
-      try_candidates = false;
+    for (int j = 0; j < 8; ++j) {
+      ckey[j * kTkThreads + tid] = sk[j];  // (the select ignores the order)
+      lo = min(lo, sk[j]);
+      hi = max(hi, sk[j]);
     }
+    const float p = (float)k / (float)n;
+    const float want = (float)kSample * p + 3.f * sqrtf((float)kSample * p * (1.f - p)) + 2.f;
+    const int r = min(kSample, max(1, (int)ceilf(want)));
+    const Selection s = block_select([&](int i) { return ckey[i]; }, kSample, r, lo, hi, sc);
+    return key_value(s.tau);
+  };
+  // 1'. or, cheaper, the threshold extrapolated from the CTA's last row: its
+  // count is linear in the threshold between (c, cnt) and (tau, k), and scales
+  // with the row's length; aim at k + 4 sqrt(k) candidates.  The filter's
+  // count verifies it; a miss takes the sample's threshold and filters again.
+  bool predicted = false;
+  if (try_candidates && n > cap) {
+    if (prev.ok && prev.cnt > k) {
+      const float target = (float)k + 4.f * sqrtf((float)k) + 8.f;
+      const float span = (float)(prev.cnt - k);
+      const float extra = target * (float)prev.n / (float)n - (float)prev.cnt;
+      if (fabsf(extra) <= (float)kExtrapSpans * span) {
+        c = prev.c - (prev.tau - prev.c) / span * extra;
+        predicted = true;
+      }
+    }
+    if (!predicted) {
+      if (n >= kSample)
+        c = sample_threshold();
+      else
+        try_candidates = false;
+    }
+    prev.ok = false;  // set again by a row that passes the check below
   }
 
-  if (try_candidates) {
+  for (int attempt = 0; try_candidates && attempt < 2; ++attempt) {
     // 2. the filter pass
     if (tid == 0) sc.cnt = 0;
     __syncthreads();
@@ -422,8 +464,16 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
             col = ccol[i];
           },
           cnt, s, k, n, bm, orow, sc);
+      if (n > cap) prev = {c, key_value(s.tau), cnt, n, true};
       return;
     }
+    if (!predicted) break;
+    // the extrapolated threshold missed: the sample's, and a second pass
+    predicted = false;
+    if (n >= kSample)
+      c = sample_threshold();
+    else
+      break;
   }
   // the same exact selection over the whole row in global memory
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
@@ -467,6 +517,7 @@ __global__ void __launch_bounds__(kTkThreads, kTkMinBlocks)
   // rows in reverse (long causal rows sit at the end), in turn over the CTAs
   int i = blockIdx.x;
   int n = length_of(i);
+  TkPrev prev{0.f, 0.f, 0, 0, false};
   if (tid == 0 && n > k) prefetch_row_l2(logits + (int64_t)(n_rows - 1 - i) * stride, n);
   for (; i < n_rows; i += gridDim.x) {
     const int row = n_rows - 1 - i;
@@ -479,7 +530,7 @@ __global__ void __launch_bounds__(kTkThreads, kTkMinBlocks)
       const float *next_x =
           n_next > k ? logits + (int64_t)(n_rows - 1 - i_next) * stride : nullptr;
       select_row(logits + (int64_t)row * stride, n, k, cap, orow, ckey, ccol, bm, sc, next_x,
-                 n_next);
+                 n_next, prev);
     }
     if (n <= k && n_next > k && tid == 0)
       prefetch_row_l2(logits + (int64_t)(n_rows - 1 - i_next) * stride, n_next);

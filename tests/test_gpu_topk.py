@@ -51,6 +51,27 @@ def test_random_lengths_every_path():
     _case(lens, 20000, 512, "normal", 2)
 
 
+def test_row_to_row_scale_changes_take_the_sample():
+    """A CTA's threshold for a row is extrapolated from its previous row and
+    checked by the filter's count; rows whose scale and offset change at
+    random (x 1000, +- 40) make that guess miss, so those rows take the
+    sampled threshold and a second filter pass -- the lists stay exact."""
+    n_rows, width, k = 3000, 12000, 512
+    x = synth.indexer_logits(n_rows, width, seed=21, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(21)
+    big = torch.rand((n_rows, 1), generator=g, device="cuda") < 0.5
+    shift = (torch.rand((n_rows, 1), generator=g, device="cuda") - 0.5) * 80.0
+    x = (torch.where(big, x * 1000.0, x) + shift).contiguous()
+    rl = torch.as_tensor(np.linspace(width, k + 1, n_rows).astype(np.int32), device="cuda")
+    got = cpmla.mla_topk_select(x, rl, k)
+    torch.cuda.synchronize()
+    assert cpmla.device_status() == 0
+    want = orc.topk_select(x.cpu().numpy(), rl.cpu().numpy(), k)
+    g_ = got.cpu().numpy()
+    bad = np.nonzero((g_ != want).any(axis=1))[0]
+    assert bad.size == 0, "rows %s differ" % bad[:5]
+
+
 def test_ties_overflow_the_candidates():
     # seven distinct values and k = 16: the top value alone fills a seventh
     # of a row, beyond the 2k + 2048 candidates for rows over 14560, so the
