@@ -50,8 +50,12 @@ def test_dense_ragged_multi_tile_every_token():
     _check_all(prob)
 
 
-@pytest.mark.parametrize("H", [1, 5, 32, 64, 128])
+@pytest.mark.parametrize("H", [1, 5, 8, 24, 32, 40, 64, 128])
 def test_dense_head_groupings(H):
+    """Heads per work item: hc = H (at most 64) over 64 // hc tokens.  A
+    multiple of 8 takes Q by TMA: 8 (eight tokens), 24 (48 of 64 rows, the
+    rest zero padding), 40 (one token, 24 padding rows); others load Q
+    through registers."""
     prob = synth.make_problem("dense_s8192_h16_p2", S=300, H=H, P=3, device="cuda", seed=H)
     _check_all(prob)
 
@@ -203,6 +207,7 @@ def test_kv_split_partials_merge_to_full_attention():
 # ------------------------------------------------ merge folded into attention
 @pytest.mark.parametrize("name,kw", [
     ("dense_s8192_h16_p2", dict(S=1000, seed=21)),
+    ("dense_s8192_h16_p2", dict(S=700, H=24, seed=26)),
     ("sparse_s32k_h32_p4", dict(S=3000, seed=22)),
     ("sparse_s128k_h16_p2_fp8", dict(S=2600, seed=23)),
     ("varlen_p8_h64", dict(prefill_lens=[2500, 1100], decode_ctx=[4100, 9000], seed=24)),
