@@ -507,21 +507,32 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
     const int nv = (n + 3) >> 2;
     for (int base = 0; base < nv; base += kTkThreads * kFilterUnroll) {
       float4 v[kFilterUnroll];
-#pragma unroll
-      for (int u = 0; u < kFilterUnroll; ++u) {
-        const int vi = base + u * kTkThreads + tid;
-        v[u] = vi < nv ? __ldcs(x4 + vi) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      }
-      // this thread's candidates; a whole iteration inside the row needs no
-      // bounds checks
       const bool whole = 4 * (base + kTkThreads * kFilterUnroll) <= n;
+      {
+        // logits past the row's end read as NaN, which no threshold passes,
+        // so the tests below need no bounds checks (0.982 ms against 0.997
+        // with a check on each element)
+        const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int u = 0; u < kFilterUnroll; ++u) {
+          const int vi = base + u * kTkThreads + tid;
+          v[u] = vi < nv ? __ldcs(x4 + vi) : make_float4(nan, nan, nan, nan);
+        }
+        if (!whole) {
+#pragma unroll
+          for (int u = 0; u < kFilterUnroll; ++u) {
+            const int j = 4 * (base + u * kTkThreads + tid);
+            if (j + 1 >= n) v[u].y = nan;
+            if (j + 2 >= n) v[u].z = nan;
+            if (j + 3 >= n) v[u].w = nan;
+          }
+        }
+      }
+      // this thread's candidates
       int q = 0;
 #pragma unroll
-      for (int u = 0; u < kFilterUnroll; ++u) {
-        const int j = 4 * (base + u * kTkThreads + tid);
-        q += (int)((whole || j < n) && v[u].x >= c) + (int)((whole || j + 1 < n) && v[u].y >= c) +
-             (int)((whole || j + 2 < n) && v[u].z >= c) + (int)((whole || j + 3 < n) && v[u].w >= c);
-      }
+      for (int u = 0; u < kFilterUnroll; ++u)
+        q += (int)(v[u].x >= c) + (int)(v[u].y >= c) + (int)(v[u].z >= c) + (int)(v[u].w >= c);
       const int total = __reduce_add_sync(0xffffffffu, q);
       int wbase = 0;
       if (lane == 0 && total) wbase = atomicAdd(&sc.cnt, total);
@@ -539,7 +550,7 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
           const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const bool pass = (whole || j + t < n) && e[t] >= c;
+            const bool pass = e[t] >= c;
             const uint32_t bal = __ballot_sync(0xffffffffu, pass);
             if (pass) {
               const uint32_t key = order_key(e[t]);
