@@ -47,15 +47,19 @@ namespace {
 constexpr int kTkThreads = 256;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kSample = 2048;     // sampled logits: one group of 8 per thread
-constexpr int kFilterUnroll = 2;  // float4 loads per thread in flight in the filter pass
+// float4 loads per thread in flight in the filter pass: with the lean appends
+// three fit the 40 registers of six CTAs per SM (2, 3, 4: 0.981, 0.954, 0.989
+// ms on the 32768-row case)
+constexpr int kFilterUnroll = 3;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kRankDirect = 64;   // a bin this small is finished by direct ranking
 constexpr int kDigitBits = 8;     // radix digit: 256 bins, one per thread in the scan
 constexpr int kBins = 1 << kDigitBits;
 constexpr int kPrefetchChunk = 32768;
-// Six CTAs per SM (the candidate arrays sized k + k/2 + 512, two loads in
-// flight per thread): 1.279 ms on the 32768-row case against 1.302 with four
-// (2k + 1024, four loads); five and eight were no faster.
+// Six CTAs per SM (the candidate arrays sized k + k/2 + 512): 1.279 ms on the
+// 32768-row case against 1.302 with four (2k + 1024, four loads), when the
+// filter kept two loads in flight; five were no faster then, nor now (three
+// loads: 0.958 against 0.954 ms).
 constexpr int kTkMinBlocks = 6;
 // A row's threshold is extrapolated from the CTA's previous row when it lies
 // within this many times the previous row's (c, tau) span of counts (2, 4, 8,
