@@ -39,7 +39,7 @@ METRIC = "CP-prefill MLA attention TFLOP/s + tokens/s (incl. merge), % of GB300 
 # capture summarised in profiles/ (per workload and path; None = not captured
 # for the current kernel).  Must be reset whenever that kernel changes.
 NCU_TRAFFIC_BYTES = {("dense_s8192_h16_p2", "merged"): 162_865_408 + 95_957_760,
-                     ("topk_s32k_k2048", "topk"): 2_241_892_096 + 258_627_328,
+                     ("topk_s32k_k2048", "topk"): 2_245_461_504 + 257_710_080,
                      # 16002-token capture of the same shape (1.433 + 1.018 GB),
                      # scaled to the workload's 326209 tokens
                      ("varlen_p8_h64", "merged"): int((1.432820e9 + 1.018263e9) * 326209 / 16002),
