@@ -73,6 +73,10 @@ constexpr int kExtrapSpans = 8;
 // 1.060, 1.055, 1.056, 1.060 ms on the 32768-row case; radix select alone
 // 1.069).
 constexpr int kRangeHalf = 128;
+// An extrapolated threshold aims at k + kTargetSigmas sqrt(k) + 8 candidates
+// (2, 3, 4, 5: 1.035, 0.984, 0.955, 0.958 ms on the 32768-row case; below 4
+// the misses' second filter passes cost more than the fewer candidates save).
+constexpr int kTargetSigmas = 4;
 
 static_assert(kSample == 8 * kTkThreads, "one sample group of 8 logits per thread");
 static_assert(kBins == kTkThreads, "one histogram bin per thread when clearing");
@@ -487,7 +491,7 @@ __device__ __forceinline__ void select_row(const float *__restrict__ x, int n, i
       (prev.ok && prev.cnt > k) ? (prev.tau - prev.c) / (float)(prev.cnt - k) : -1.f;
   if (try_candidates && n > cap) {
     if (prev.ok && prev.cnt > k) {
-      const float target = (float)k + 4.f * sqrtf((float)k) + 8.f;
+      const float target = (float)k + (float)kTargetSigmas * sqrtf((float)k) + 8.f;
       const float span = (float)(prev.cnt - k);
       const float extra = target * (float)prev.n / (float)n - (float)prev.cnt;
       if (fabsf(extra) <= (float)kExtrapSpans * span) {
